@@ -1,0 +1,361 @@
+"""Throughput benchmark: causal GQA attention forward + backward on one GB300.
+
+One step = one pass of the whole path over one batch of the GPT-2-small
+attention workload (B=8, H=12, Hkv=4, N=1024, d=64, bf16 inputs, fp32 LSE and
+accumulation): forward (O, LSE), backward preprocess, backward main kernel,
+dQ cast.  Inputs are synthetic (seeded), resident in HBM before the timed
+region.  The working set (~70 MB) is smaller than L2, so L2 is flushed
+(a 256 MiB write) between timed steps, outside each step's events.
+
+Prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle instead
+(on a bounded sample of the same workload, on the host cores).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "causal GQA attention fwd+bwd TFLOP/s and % of GB300 bf16 tensor peak"
+WORKLOAD = "gpt2s_bf16"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_config(w, extra=None):
+    cfg = {"workload": f"causal GQA attention fwd+bwd, GPT-2-small shape "
+                       f"B={w.B} H={w.H} Hkv={w.Hkv} N={w.N} d={w.d} {w.dtype}",
+           "B": w.B, "H": w.H, "Hkv": w.Hkv, "N": w.N, "d": w.d, "causal": w.causal,
+           "scale": w.scale, "inputs": "seeded synthetic: Q,K,V,dO ~ N(0,1), seed 0",
+           "l2": "flushed between timed steps (256 MiB write), outside the step events",
+           "parallelism": "replicas"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+def kernel_file_hash():
+    h = hashlib.sha256()
+    for f in ("bwd.cu", "fwd.cu", "ptx.cuh"):
+        h.update(open(os.path.join(ROOT, "causal_gqa_flashattention_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernels have changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("kernel_hash") != kernel_file_hash():
+        return None
+    return d.get("per_launch_bytes", {}).get(kernel)
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_cuda(args):
+    import torch
+    from causal_gqa_flashattention_gb300 import nea
+    from causal_gqa_flashattention_gb300.workloads import WORKLOADS, make_inputs
+
+    ws, rank, local = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[WORKLOAD]
+    nea.lib()
+    q, k, v, do = make_inputs(w, seed=0, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    wsb = nea.bwd_workspace_bytes(w.B, w.H, w.Hkv, w.N, w.d, nea.NEA_BF16)
+    wsp = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        nea.attn_fwd(q, k, v, causal=True, scale=w.scale, out=o, lse=lse, stream=stream)
+        nea.attn_bwd_stages(q, k, v, o, do, lse, dq, dk, dv, wsp, causal=True, scale=w.scale,
+                            stream=stream,
+                            between=(lambda i: evs[i + 1].record(stream)) if evs else None)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if nea.check_status(stream) != nea.NEA_OK:
+        raise RuntimeError("kernel status word set during warm-up")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        for i in range(K):
+            flush.zero_()
+            step(evs[i])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    barrier(ws)
+    if nea.check_status(stream) != nea.NEA_OK:
+        raise RuntimeError("kernel status word set during the timed region")
+    per = [[evs[i][s].elapsed_time(evs[i][s + 1]) for s in range(4)] for i in range(K)]
+    # per[i] = [fwd, bwd_pre, bwd_main, bwd_post] in ms
+    step_ms = [sum(p) for p in per]
+    ms_step = max_over_ranks(sum(step_ms) / K, ws)
+    flops = w.fwd_flops() + w.bwd_flops()
+    value = ws * flops / (ms_step * 1e-3) / 1e12
+    k_ms = [sum(p[s] for p in per) / K for s in range(4)]
+    peaks, src = load_peaks()
+    peak_tc = float(peaks["bf16_tflops"])
+    peak_hbm = float(peaks["hbm_gbs"])
+
+    # end to end through the public calls, with pinned host buffers: H2D of
+    # q,k,v,dO, fwd, bwd, D2H of dQ,dK,dV, all inside each step's events
+    hin = [t.cpu().pin_memory() for t in (q, k, v, do)]
+    hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv)]
+    dq2, dk2, dv2 = torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv)
+    din = [torch.empty_like(t) for t in (q, k, v, do)]
+    bi = sum(t.numel() * t.element_size() for t in hin)
+    bo = sum(t.numel() * t.element_size() for t in hout)
+
+    def e2e_step():
+        for d_, h_ in zip(din, hin):
+            d_.copy_(h_, non_blocking=True)
+        o2, l2 = nea.attn_fwd(din[0], din[1], din[2], causal=True, scale=w.scale, stream=stream)
+        nea.attn_bwd(din[0], din[1], din[2], o2, din[3], l2, causal=True, scale=w.scale,
+                     dq=dq2, dk=dk2, dv=dv2, workspace=wsp, stream=stream)
+        for h_, d_ in zip(hout, (dq2, dk2, dv2)):
+            h_.copy_(d_, non_blocking=True)
+
+    for _ in range(max(args.warmup, 3)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_ms = []
+    for _ in range(K):
+        flush.zero_()
+        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_.record(stream)
+        e2e_step()
+        b_.record(stream)
+        b_.synchronize()
+        e_ms.append(a_.elapsed_time(b_))
+    e_ms_step = max_over_ranks(sum(e_ms) / K, ws)
+
+    main_flops = w.bwd_flops()
+    main_tf = main_flops / (k_ms[2] * 1e-3) / 1e12
+    rows = w.B * w.H * w.N
+    pre_bytes = 2 * rows * w.d * w.esize + rows * 4 + 2 * rows * 4 + rows * w.d * 4
+    post_bytes = rows * w.d * 4 + rows * w.d * w.esize
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": workload_config(w),
+        "pct_of_peak": round(100.0 * value / ws / peak_tc, 2),
+        "roofline": {"kernel": "bwd_main", "bound": "tensor", "achieved": round(main_tf, 1),
+                     "peak": peak_tc, "unit": "TFLOP/s", "frac": round(main_tf / peak_tc, 4),
+                     "peak_source": f"bf16_tflops (burst) of {src}",
+                     "traffic": traffic_for("bwd_main")},
+        "kernels": {
+            "fwd": {"ms": round(k_ms[0], 5),
+                    "tflops": round(w.fwd_flops() / (k_ms[0] * 1e-3) / 1e12, 1)},
+            "bwd_pre": {"ms": round(k_ms[1], 5),
+                        "gbs": round(pre_bytes / (k_ms[1] * 1e-3) / 1e9, 1),
+                        "hbm_frac": round(pre_bytes / (k_ms[1] * 1e-3) / 1e9 / peak_hbm, 3)},
+            "bwd_main": {"ms": round(k_ms[2], 5), "tflops": round(main_tf, 1)},
+            "bwd_post": {"ms": round(k_ms[3], 5),
+                         "gbs": round(post_bytes / (k_ms[3] * 1e-3) / 1e9, 1)},
+        },
+        "e2e": {"value": round(ws * flops / (e_ms_step * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e_ms_step, 4), "h2d_bytes_per_step": bi,
+                "d2h_bytes_per_step": bo},
+        "gpu_launches": 4 * K,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": round(wall, 4),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, seconds=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def oracle_sample(w, nb):
+    """A bounded sample of the workload: the first `nb` batch elements."""
+    from causal_gqa_flashattention_gb300.workloads import make_inputs
+    q, k, v, do = make_inputs(w, seed=0)
+    return q[:nb], k[:nb], v[:nb], do[:nb]
+
+
+def cpu_baseline(w, seconds=10.0, nb=1):
+    import oracle
+    q, k, v, do = oracle_sample(w, nb)
+    flops = (w.fwd_flops() + w.bwd_flops()) * nb / w.B
+    runs = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.attn_fwd(q, k, v, w.scale, True)
+        oracle.attn_bwd(q, k, v, do, w.scale, True)
+        runs += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = (time.perf_counter() - t0) / runs
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"batch element(s) 0..{nb - 1} of {w.B} (B={nb}, H={w.H}, Hkv={w.Hkv}, "
+                      f"N={w.N}, d={w.d}), fwd+bwd in fp64, {runs} run(s), "
+                      f"{dt:.2f} s per run; causal FLOPs counted as on the GPU"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from causal_gqa_flashattention_gb300.workloads import WORKLOADS
+    import oracle
+    w = WORKLOADS[WORKLOAD]
+    nb = 1
+    q, k, v, do = oracle_sample(w, nb)
+    flops = (w.fwd_flops() + w.bwd_flops()) * nb / w.B
+    for _ in range(args.warmup):
+        oracle.attn_fwd(q[:, :, :128], k[:, :, :128], v[:, :, :128], w.scale, True)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.attn_fwd(q, k, v, w.scale, True)
+        oracle.attn_bwd(q, k, v, do, w.scale, True)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = flops / (ms * 1e-3) / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w, {"sample": f"batch element 0 of {w.B} per step"}),
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "kind": "oracle",
+                             "cores": oracle.num_threads(),
+                             "sample": f"B=1 of the B={w.B} workload per step, fp64 oracle"},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "cuda":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_cuda(args)
+
+
+if __name__ == "__main__":
+    main()

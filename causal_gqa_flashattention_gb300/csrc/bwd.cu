@@ -1,0 +1,566 @@
+// bwd.cu -- causal grouped-query FlashAttention backward on tcgen05 / TMEM.
+//
+// "NanoEuler: Hand-writing GPT-2 in Pure C/CUDA", section "Hand-written
+// Backpropagation": every gradient is derived and written by hand.  For
+// softmax attention with upstream dO:
+//   dV = P^T dO,  dP = dO V^T,  dS = P o (dP - D),  D = rowsum(dO o O),
+//   dQ = scale dS K,  dK = scale dS^T Q,  P recomputed from the saved LSE.
+//
+// Three kernels:
+//  bwd_pre   (HBM-bound)  Ds = scale * rowsum(dO o O), L2 = LSE * log2(e),
+//                         and zeroes the fp32 dQ accumulator;
+//  bwd_main  one CTA per (batch, KV head, 128-row key tile j); it walks the
+//            group's query heads and the query tiles i >= j (causal):
+//              warp 0      TMA producer (K_j, V_j once; Q_i, dO_i, L2_i, Ds_i
+//                          per step into a ring)
+//              warp 1      MMA issuer + TMEM owner
+//              warps 4..7  "compute": thread = key row; P^T = exp2(S^T c - L2)
+//                          to TMEM (bf16), dS^T = P^T o (scale dP^T - Ds) to
+//                          smem (bf16, 128-B swizzle)
+//              warps 8..11 "dQ": thread = query row; dQ_i partial TMEM ->
+//                          smem -> TMA reduce-add (fp32) into the accumulator
+//            MMAs per step: S^T = K Q^T, dP^T = V dO^T (both SS, K-major),
+//            dV += P^T dO (TS), dK += dS^T Q (SS, B MN-major),
+//            dQ = dS K (SS, A and B MN-major; same smem bytes as dS^T).
+//            dK and dV stay in TMEM for the whole CTA: the sum over the
+//            group's query heads needs no atomics.
+//  bwd_post  dQ = bf16(dQ accumulator).
+#include "nea_internal.h"
+#include "ptx.cuh"
+
+namespace nea {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------- preprocess
+// TPR threads per row, each owning 16 bytes of O and dO.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const T* __restrict__ O,
+                                                      const T* __restrict__ dO,
+                                                      const float* __restrict__ lse,
+                                                      float* __restrict__ ds_row,
+                                                      float* __restrict__ l2_row,
+                                                      float* __restrict__ dq_acc, long long rows,
+                                                      float scale) {
+  constexpr int EPV = 16 / sizeof(T);  // elements per 16-B vector
+  constexpr int TPR = D / EPV;         // threads per row
+  constexpr int RPB = 256 / TPR;       // rows per block-iteration
+  const int sub = threadIdx.x % TPR;
+  for (long long row = static_cast<long long>(blockIdx.x) * RPB + threadIdx.x / TPR; row < rows;
+       row += static_cast<long long>(gridDim.x) * RPB) {
+    const size_t base = static_cast<size_t>(row) * D + sub * EPV;
+    const uint4 ov = __ldg(reinterpret_cast<const uint4*>(O + base));
+    const uint4 gv = __ldg(reinterpret_cast<const uint4*>(dO + base));
+    float acc = 0.f;
+    if constexpr (sizeof(T) == 2) {
+      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 a = __bfloat1622float2(o2[k]), b = __bfloat1622float2(g2[k]);
+        acc = fmaf(a.x, b.x, acc);
+        acc = fmaf(a.y, b.y, acc);
+      }
+    } else {
+      const float* o4 = reinterpret_cast<const float*>(&ov);
+      const float* g4 = reinterpret_cast<const float*>(&gv);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc = fmaf(o4[k], g4[k], acc);
+    }
+#pragma unroll
+    for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (sub == 0) {
+      ds_row[row] = acc * scale;
+      l2_row[row] = lse[row] * kLog2e;
+    }
+    // zero this thread's share of the fp32 accumulator row (D floats)
+    float4* z = reinterpret_cast<float4*>(dq_acc + static_cast<size_t>(row) * D);
+#pragma unroll
+    for (int k = sub; k < D / 4; k += TPR) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// ---------------------------------------------------------------- dQ cast
+__global__ void __launch_bounds__(256) bwd_post_kernel(const float* __restrict__ acc,
+                                                       __nv_bfloat16* __restrict__ dq,
+                                                       long long n8) {
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i);
+    const float4 b = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i + 1);
+    uint4 v;
+    v.x = pack_bf16(a.x, a.y);
+    v.y = pack_bf16(a.z, a.w);
+    v.z = pack_bf16(b.x, b.y);
+    v.w = pack_bf16(b.z, b.w);
+    reinterpret_cast<uint4*>(dq)[i] = v;
+  }
+}
+
+// ---------------------------------------------------------------- main
+template <int D>
+struct BwdCfg {
+  static constexpr int ES = 2;
+  static constexpr int NBLK = D / 64;
+  static constexpr int BLK_BYTES = kTile * 128;
+  static constexpr int TILE_BYTES = NBLK * BLK_BYTES;
+  static constexpr int QST = D == 64 ? 2 : 1;  // Q / dO ring depth
+  static constexpr int NK_QK = D / 16;           // K-steps over d
+  static constexpr int NK_T = kTile / 16;        // K-steps over 128 rows
+  // tensor memory columns
+  static constexpr int S_COL = 0, DP_COL = 128, DV_COL = 256;
+  static constexpr int DK_COL = D == 64 ? 320 : 384;
+  static constexpr int DQ_COL = D == 64 ? 384 : 128;  // d=128: shares dP's columns
+  static constexpr int P_COL = D == 64 ? 448 : 0;     // d=128: shares S's columns
+  static constexpr bool DQ_ALIAS_DP = D == 128;
+  // shared memory (offsets from the 1024-B aligned base)
+  static constexpr int OFF_K = 0, OFF_V = TILE_BYTES, OFF_Q = 2 * TILE_BYTES;
+  static constexpr int OFF_DO = OFF_Q + QST * TILE_BYTES;
+  static constexpr int OFF_DS = OFF_DO + QST * TILE_BYTES;  // 128x128 bf16, 2 blocks
+  static constexpr int OFF_DQ = OFF_DS + 2 * BLK_BYTES;      // 2 fp32 boxes of 128x32
+  static constexpr int OFF_L2 = OFF_DQ + 2 * BLK_BYTES;
+  static constexpr int OFF_DSR = OFF_L2 + QST * 512;
+  static constexpr int SMEM_BYTES = 1024 + OFF_DSR + QST * 512;
+  static constexpr int THREADS = 384;
+};
+
+enum : int {
+  C_KVFULL = 0, C_SFULL, C_DPFULL, C_PFULL, C_DSFULL, C_DSEMPTY, C_DQFULL, C_DQFREE, C_FINAL,
+  C_DRAIN, C_QFULL  // then QFULL[QST], DOFULL[QST], QEMPTY[QST]
+};
+
+template <int D>
+__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const __grid_constant__ BwdArgs a) {
+  using C = BwdCfg<D>;
+  constexpr int QST = C::QST;
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  __shared__ __align__(8) uint64_t bars[C_QFULL + 3 * QST];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = a.N / kTile;
+  const int BG = a.B * a.Hkv;
+  const int G = a.H / a.Hkv;
+  const int lin = blockIdx.x;
+  const int j = lin / BG;  // key tile; j = 0 has the most query tiles under the causal mask
+  const int bg = lin % BG;
+  const int b = bg / a.Hkv, g = bg % a.Hkv;
+  const int i0 = a.causal ? j : 0;
+  const int nI = T - i0;
+  const int nsteps = G * nI;
+
+  const uint32_t base = smem_u32(smem);
+  const uint32_t sK = base + C::OFF_K, sV = base + C::OFF_V, sDS = base + C::OFF_DS,
+                 sDQ = base + C::OFF_DQ;
+  auto sQ = [&](int s) { return base + C::OFF_Q + s * C::TILE_BYTES; };
+  auto sDO = [&](int s) { return base + C::OFF_DO + s * C::TILE_BYTES; };
+  const float* l2_s = reinterpret_cast<const float*>(smem + C::OFF_L2);
+  const float* dsr_s = reinterpret_cast<const float*>(smem + C::OFF_DSR);
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  auto qfull = [&](int s) { return bar(C_QFULL + s); };
+  auto dofull = [&](int s) { return bar(C_QFULL + QST + s); };
+  auto qempty = [&](int s) { return bar(C_QFULL + 2 * QST + s); };
+  volatile int* abort = &abort_sh;
+  unsigned int* status = a.status;
+
+  if (threadIdx.x == 0) {
+    abort_sh = 0;
+    mbar_init(bar(C_KVFULL), 1);
+    mbar_init(bar(C_SFULL), 1);
+    mbar_init(bar(C_DPFULL), 1);
+    mbar_init(bar(C_PFULL), 128);
+    mbar_init(bar(C_DSFULL), 128);
+    mbar_init(bar(C_DSEMPTY), 1);
+    mbar_init(bar(C_DQFULL), 1);
+    mbar_init(bar(C_DQFREE), 128);
+    mbar_init(bar(C_FINAL), 1);
+    mbar_init(bar(C_DRAIN), 1);
+    for (int s = 0; s < QST; ++s) {
+      mbar_init(qfull(s), 1);
+      mbar_init(dofull(s), 1);
+      mbar_init(qempty(s), 1 + 4);  // MMA commit + one arrive per compute warp
+    }
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&a.tmQ);
+    prefetch_tmap(&a.tmK);
+    prefetch_tmap(&a.tmV);
+    prefetch_tmap(&a.tmdO);
+    prefetch_tmap(&a.tmdQacc);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_base_sh), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  auto step_hi = [&](int n, int& h, int& i) {
+    h = g * G + n / nI;
+    i = i0 + n % nI;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const int kvh = b * a.Hkv + g;
+      mbar_expect_tx(bar(C_KVFULL), 2 * C::TILE_BYTES);
+      for (int k = 0; k < C::NBLK; ++k) {
+        tma_load_3d(sK + k * C::BLK_BYTES, &a.tmK, bar(C_KVFULL), k * 64, j * kTile, kvh);
+        tma_load_3d(sV + k * C::BLK_BYTES, &a.tmV, bar(C_KVFULL), k * 64, j * kTile, kvh);
+      }
+      int issued = 0;
+      bool ok = true;
+      for (int n = 0; n < nsteps; ++n) {
+        const int s = n % QST;
+        if (n >= QST && !mbar_wait(qempty(s), ((n / QST) - 1) & 1, abort, 20, status)) {
+          ok = false;
+          break;
+        }
+        int h, i;
+        step_hi(n, h, i);
+        const int bh = b * a.H + h;
+        const size_t row0 = static_cast<size_t>(bh) * a.N + static_cast<size_t>(i) * kTile;
+        mbar_expect_tx(qfull(s), C::TILE_BYTES + 512);
+        for (int k = 0; k < C::NBLK; ++k)
+          tma_load_3d(sQ(s) + k * C::BLK_BYTES, &a.tmQ, qfull(s), k * 64, i * kTile, bh);
+        bulk_load(base + C::OFF_L2 + s * 512, a.lse2 + row0, 512, qfull(s));
+        mbar_expect_tx(dofull(s), C::TILE_BYTES + 512);
+        for (int k = 0; k < C::NBLK; ++k)
+          tma_load_3d(sDO(s) + k * C::BLK_BYTES, &a.tmdO, dofull(s), k * 64, i * kTile, bh);
+        bulk_load(base + C::OFF_DSR + s * 512, a.delta + row0, 512, dofull(s));
+        issued = n + 1;
+      }
+      mbar_wait_drain(bar(C_KVFULL), 0, 21, status);
+      if (!ok) {
+        for (int n = issued - QST > 0 ? issued - QST : 0; n < issued; ++n) {
+          mbar_wait_drain(qfull(n % QST), (n / QST) & 1, 21, status);
+          mbar_wait_drain(dofull(n % QST), (n / QST) & 1, 21, status);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = make_idesc<MmaKind::kBF16>(128, 128, false, false);
+      constexpr uint32_t idDV = make_idesc<MmaKind::kBF16>(128, D, false, true);
+      constexpr uint32_t idDK = make_idesc<MmaKind::kBF16>(128, D, false, true);
+      constexpr uint32_t idDQ = make_idesc<MmaKind::kBF16>(128, D, true, true);
+      bool ok = mbar_wait(bar(C_KVFULL), 0, abort, 22, status);
+      for (int n = 0; ok && n < nsteps; ++n) {
+        const int s = n % QST;
+        const uint32_t ph = (n / QST) & 1;
+        // S^T = K_j Q_i^T
+        if (!mbar_wait(qfull(s), ph, abort, 23, status)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < C::NK_QK; ++k) {
+          const uint32_t off = (k / 4) * C::BLK_BYTES + (k % 4) * 32;
+          mma_ss<MmaKind::kBF16>(tmem + C::S_COL, sdesc_sw128(sK + off, 16, 1024),
+                                 sdesc_sw128(sQ(s) + off, 16, 1024), idS, k > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(C_SFULL));
+        // dP^T = V_j dO_i^T
+        if (!mbar_wait(dofull(s), ph, abort, 24, status)) break;
+        if (C::DQ_ALIAS_DP && n > 0 && !mbar_wait(bar(C_DQFREE), (n - 1) & 1, abort, 25, status))
+          break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < C::NK_QK; ++k) {
+          const uint32_t off = (k / 4) * C::BLK_BYTES + (k % 4) * 32;
+          mma_ss<MmaKind::kBF16>(tmem + C::DP_COL, sdesc_sw128(sV + off, 16, 1024),
+                                 sdesc_sw128(sDO(s) + off, 16, 1024), idS, k > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(C_DPFULL));
+        // dV += P^T dO_i
+        if (!mbar_wait(bar(C_PFULL), n & 1, abort, 26, status)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < C::NK_T; ++k)
+          mma_ts<MmaKind::kBF16>(tmem + C::DV_COL, tmem + C::P_COL + k * 8,
+                                 sdesc_sw128(sDO(s) + k * 16 * 128, C::BLK_BYTES, 1024), idDV,
+                                 (n > 0 || k > 0) ? 1u : 0u);
+        // dK += dS^T Q_i ; dQ_i = dS K_j
+        if (!mbar_wait(bar(C_DSFULL), n & 1, abort, 27, status)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < C::NK_T; ++k) {
+          const uint32_t off = (k / 4) * C::BLK_BYTES + (k % 4) * 32;
+          mma_ss<MmaKind::kBF16>(tmem + C::DK_COL, sdesc_sw128(sDS + off, 16, 1024),
+                                 sdesc_sw128(sQ(s) + k * 16 * 128, C::BLK_BYTES, 1024), idDK,
+                                 (n > 0 || k > 0) ? 1u : 0u);
+        }
+        mma_commit(qempty(s));
+        if (!C::DQ_ALIAS_DP && n > 0 && !mbar_wait(bar(C_DQFREE), (n - 1) & 1, abort, 28, status))
+          break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < C::NK_T; ++k)
+          mma_ss<MmaKind::kBF16>(tmem + C::DQ_COL,
+                                 sdesc_sw128(sDS + k * 16 * 128, C::BLK_BYTES, 1024),
+                                 sdesc_sw128(sK + k * 16 * 128, C::BLK_BYTES, 1024), idDQ,
+                                 k > 0 ? 1u : 0u);
+        mma_commit(bar(C_DSEMPTY));
+        mma_commit(bar(C_DQFULL));
+      }
+      mma_commit(bar(C_FINAL));
+      mma_commit(bar(C_DRAIN));
+      mbar_wait_drain(bar(C_DRAIN), 0, 29, status);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ compute
+    const int quad = warp & 3;
+    const int kr = quad * 32 + lane;  // key row within tile j == TMEM lane
+    const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const float c = a.scale * kLog2e;
+    bool ok = true;
+    for (int n = 0; n < nsteps; ++n) {
+      const int s = n % QST;
+      const uint32_t ph = (n / QST) & 1;
+      int h, i;
+      step_hi(n, h, i);
+      if (!mbar_wait_warp(qfull(s), ph, abort, 30, status) ||
+          !mbar_wait_warp(bar(C_SFULL), n & 1, abort, 31, status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t u0[32], u1[32], u2[32], u3[32];
+      tmem_ld32(trow + C::S_COL + 0, u0);
+      tmem_ld32(trow + C::S_COL + 32, u1);
+      tmem_ld32(trow + C::S_COL + 64, u2);
+      tmem_ld32(trow + C::S_COL + 96, u3);
+      tmem_ld_wait(u0);
+      reg_fence(u1);
+      reg_fence(u2);
+      reg_fence(u3);
+      const float* l2 = l2_s + s * 128;
+      const bool diag = a.causal && i == j;
+      uint32_t pk[64];  // P^T row, bf16 pairs (query 2t in the low half)
+      auto make_p = [&](const uint32_t (&u)[32], int c0) {
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const float2 lv = *reinterpret_cast<const float2*>(l2 + c0 + 2 * t);
+          float p0 = ex2(fmaf(__uint_as_float(u[2 * t]), c, -lv.x));
+          float p1 = ex2(fmaf(__uint_as_float(u[2 * t + 1]), c, -lv.y));
+          if (diag) {
+            if (c0 + 2 * t < kr) p0 = 0.f;
+            if (c0 + 2 * t + 1 < kr) p1 = 0.f;
+          }
+          pk[c0 / 2 + t] = pack_bf16(p0, p1);
+        }
+      };
+      make_p(u0, 0);
+      make_p(u1, 32);
+      make_p(u2, 64);
+      make_p(u3, 96);
+      {
+        uint32_t w[32];
+#pragma unroll
+        for (int t = 0; t < 32; ++t) w[t] = pk[t];
+        tmem_st32(trow + C::P_COL, w);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) w[t] = pk[32 + t];
+        tmem_st32(trow + C::P_COL + 32, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(C_PFULL));
+      // dS^T = P^T o (scale dP^T - Ds)
+      if (!mbar_wait_warp(dofull(s), ph, abort, 32, status) ||
+          !mbar_wait_warp(bar(C_DPFULL), n & 1, abort, 33, status) ||
+          (n > 0 && !mbar_wait_warp(bar(C_DSEMPTY), (n - 1) & 1, abort, 34, status))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float* dsr = dsr_s + s * 128;
+      uint8_t* dsrow = smem + C::OFF_DS + kr * 128;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t v[32];
+        tmem_ld32(trow + C::DP_COL + 32 * cc, v);
+        tmem_ld_wait(v);
+        uint32_t o[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const int q = 32 * cc + 2 * t;
+          const uint32_t pp = pk[q / 2];
+          const float p0 = __uint_as_float(pp << 16), p1 = __uint_as_float(pp & 0xffff0000u);
+          const float2 dv = *reinterpret_cast<const float2*>(dsr + q);
+          const float d0 = p0 * fmaf(__uint_as_float(v[2 * t]), a.scale, -dv.x);
+          const float d1 = p1 * fmaf(__uint_as_float(v[2 * t + 1]), a.scale, -dv.y);
+          o[t] = pack_bf16(d0, d1);
+        }
+        // 32 queries -> 64 B of row kr: block (32cc)/64, chunks 4*(cc%2) .. +3
+        const int blk = cc / 2;
+#pragma unroll
+        for (int t4 = 0; t4 < 4; ++t4) {
+          const int chunk = 4 * (cc % 2) + t4;
+          *reinterpret_cast<uint4*>(dsrow + blk * C::BLK_BYTES + ((chunk ^ (kr & 7)) << 4)) =
+              make_uint4(o[4 * t4], o[4 * t4 + 1], o[4 * t4 + 2], o[4 * t4 + 3]);
+        }
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      mbar_arrive(bar(C_DSFULL));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qempty(s));
+    }
+    // epilogue: dV, dK rows of this key tile
+    if (ok) ok = mbar_wait_warp(bar(C_FINAL), 0, abort, 35, status);
+    if (ok) {
+      tc_fence_after();
+      const size_t row = (static_cast<size_t>(b) * a.Hkv + g) * a.N + static_cast<size_t>(j) * kTile + kr;
+      __nv_bfloat16* dv_out = static_cast<__nv_bfloat16*>(a.dV) + row * D;
+      __nv_bfloat16* dk_out = static_cast<__nv_bfloat16*>(a.dK) + row * D;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        __nv_bfloat16* dst = which == 0 ? dv_out : dk_out;
+        const uint32_t col = which == 0 ? C::DV_COL : C::DK_COL;
+#pragma unroll
+        for (int cc = 0; cc < D; cc += 32) {
+          uint32_t v[32];
+          tmem_ld32(trow + col + cc, v);
+          tmem_ld_wait(v);
+#pragma unroll
+          for (int t4 = 0; t4 < 4; ++t4) {
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(v[8 * t4 + 0]), __uint_as_float(v[8 * t4 + 1]));
+            w.y = pack_bf16(__uint_as_float(v[8 * t4 + 2]), __uint_as_float(v[8 * t4 + 3]));
+            w.z = pack_bf16(__uint_as_float(v[8 * t4 + 4]), __uint_as_float(v[8 * t4 + 5]));
+            w.w = pack_bf16(__uint_as_float(v[8 * t4 + 6]), __uint_as_float(v[8 * t4 + 7]));
+            *reinterpret_cast<uint4*>(dst + cc + 8 * t4) = w;
+          }
+        }
+      }
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ dQ
+    const int quad = warp & 3;
+    const int qr = quad * 32 + lane;  // query row == TMEM lane of the dQ tile
+    const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const bool leader = warp == 8 && lane == 0;
+    bool ok = true;
+    for (int n = 0; n < nsteps; ++n) {
+      int h, i;
+      step_hi(n, h, i);
+      const int bh = b * a.H + h;
+      // the whole warpgroup unwinds together: it meets at named barriers below
+      if (!named_bar_and(2, 128, mbar_wait_warp(bar(C_DQFULL), n & 1, abort, 36, status))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int half = 0; half < D / 64; ++half) {
+        uint32_t v0[32], v1[32];
+        tmem_ld32(trow + C::DQ_COL + 64 * half, v0);
+        tmem_ld32(trow + C::DQ_COL + 64 * half + 32, v1);
+        tmem_ld_wait(v0);
+        reg_fence(v1);
+        if (half == D / 64 - 1) {
+          tc_fence_before();
+          mbar_arrive(bar(C_DQFREE));
+        }
+        // staging free once the previous reduction has read it
+        if (leader) bulk_wait_read0();
+        named_bar_sync(2, 128);
+#pragma unroll
+        for (int box = 0; box < 2; ++box) {
+          const uint32_t(&v)[32] = box == 0 ? v0 : v1;
+          uint8_t* rowp = smem + C::OFF_DQ + box * C::BLK_BYTES + qr * 128;
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)
+            *reinterpret_cast<uint4*>(rowp + ((ch ^ (qr & 7)) << 4)) =
+                make_uint4(v[4 * ch], v[4 * ch + 1], v[4 * ch + 2], v[4 * ch + 3]);
+        }
+        fence_proxy_async();
+        named_bar_sync(2, 128);
+        if (leader) {
+          for (int box = 0; box < 2; ++box)
+            tma_reduce_add_3d(&a.tmdQacc, sDQ + box * C::BLK_BYTES, 64 * half + 32 * box,
+                              i * kTile, bh);
+          bulk_commit();
+        }
+      }
+    }
+    (void)ok;
+    if (leader) bulk_wait0();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+unsigned grid_for(long long work_items, int per_block) {
+  long long blocks = (work_items + per_block - 1) / per_block;
+  const long long cap = 152LL * 16;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return static_cast<unsigned>(blocks);
+}
+
+template <int D>
+cudaError_t launch_main_t(const BwdArgs& a, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  auto kern = bwd_main_kernel<D>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = static_cast<unsigned>(a.B) * a.Hkv * (a.N / kTile);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(a.B) * a.H * a.N;
+  if (a.dtype == 0) {
+    const int tpr = a.d / 8;
+    const unsigned grid = grid_for(rows, 256 / tpr);
+    if (a.d == 64)
+      bwd_pre_kernel<__nv_bfloat16, 64><<<grid, 256, 0, stream>>>(
+          static_cast<const __nv_bfloat16*>(a.O), static_cast<const __nv_bfloat16*>(a.dO), a.lse,
+          a.delta, a.lse2, a.dq_acc, rows, a.scale);
+    else
+      bwd_pre_kernel<__nv_bfloat16, 128><<<grid, 256, 0, stream>>>(
+          static_cast<const __nv_bfloat16*>(a.O), static_cast<const __nv_bfloat16*>(a.dO), a.lse,
+          a.delta, a.lse2, a.dq_acc, rows, a.scale);
+  } else {
+    const unsigned grid = grid_for(rows, 256 / (a.d / 4));
+    if (a.d == 64)
+      bwd_pre_kernel<float, 64><<<grid, 256, 0, stream>>>(
+          static_cast<const float*>(a.O), static_cast<const float*>(a.dO), a.lse, a.delta, a.lse2,
+          a.dq_acc, rows, a.scale);
+    else
+      return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
+  if (a.dtype == 0 && a.d == 64) return launch_main_t<64>(a, stream);
+  if (a.dtype == 0 && a.d == 128) return launch_main_t<128>(a, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bwd_post(const BwdArgs& a, cudaStream_t stream) {
+  const long long n8 = static_cast<long long>(a.B) * a.H * a.N * a.d / 8;
+  bwd_post_kernel<<<grid_for(n8, 256), 256, 0, stream>>>(
+      a.dq_acc, static_cast<__nv_bfloat16*>(a.dQ), n8);
+  return cudaGetLastError();
+}
+
+}  // namespace nea

@@ -1,0 +1,360 @@
+// fwd.cu -- causal grouped-query FlashAttention forward on tcgen05 / TMEM.
+//
+// "NanoEuler: Hand-writing GPT-2 in Pure C/CUDA", section "Tiled
+// FlashAttention": one block per query tile, an outer loop over key/value
+// tiles staged in shared memory, S = Q K^T, an online softmax update, and an
+// accumulated output.  Here, per CTA = one (batch, head, 128-row query tile):
+//
+//   warp 0      TMA producer: Q once, then K_j / V_j into a 2-stage ring
+//   warp 1      MMA issuer (one thread): S = Q K_j^T (SS), O += P V_j (TS,
+//               P read from tensor memory); owns the TMEM allocation
+//   warps 2..5  softmax: thread = query row (TMEM lane); reads S with
+//               tcgen05.ld, causal mask on the diagonal tile, online max /
+//               sum in the log2 domain, writes P (bf16 or tf32) back to TMEM,
+//               rescales O only when the running max grew by more than 2^8;
+//               epilogue O / l -> smem -> TMA store, LSE -> global
+//
+// Tensor memory (fp32 columns, lane = query row): S [0,128), O [128,128+d),
+// P [128+d, ...).  Key tiles above the causal diagonal are never loaded.
+#include "nea_internal.h"
+#include "ptx.cuh"
+
+namespace nea {
+namespace {
+
+constexpr int pow2_cols(int n) {
+  return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : n <= 256 ? 256 : 512;
+}
+
+template <int D, MmaKind KIND>
+struct FwdCfg {
+  static constexpr int ES = KIND == MmaKind::kBF16 ? 2 : 4;  // element bytes
+  static constexpr int BLK_ELEMS = 128 / ES;                 // elements per 128-B row
+  static constexpr int NBLK = D * ES / 128;                  // 128-B column blocks per row
+  static constexpr int BLK_BYTES = kTile * 128;              // one column block of a tile
+  static constexpr int TILE_BYTES = NBLK * BLK_BYTES;
+  static constexpr int KPER = 32 / ES;                       // K of one MMA instruction
+  static constexpr int NK_QK = D * ES / 32;
+  static constexpr int NK_PV = kTile / KPER;
+  static constexpr int S_COL = 0, O_COL = 128, P_COL = 128 + D;
+  static constexpr int P_COLS = KIND == MmaKind::kBF16 ? 64 : 128;
+  static constexpr int TMEM_COLS = pow2_cols(P_COL + P_COLS);
+  static constexpr int CTAS_PER_SM = TMEM_COLS <= 256 ? 2 : 1;
+  static constexpr int STAGES = 2;
+  static constexpr int THREADS = 192;
+  // Q tile, then per stage: K tile, V tile.  +1 KB for 1024-B alignment.
+  static constexpr int SMEM_BYTES = 1024 + TILE_BYTES * (1 + 2 * STAGES);
+};
+
+// mbarrier slots
+enum : int { B_QFULL = 0, B_SFULL, B_SFREE, B_PFULL, B_ODONE, B_DRAIN, B_KFULL };
+// K_FULL[s] = B_KFULL + s, V_FULL[s] = B_KFULL + ST + s, KV_EMPTY[s] = B_KFULL + 2 ST + s
+
+constexpr float kLog2e = 1.4426950408889634f;
+// Lazy rescale: O and l keep a stale row max until the true max exceeds it
+// by more than this (log2 units); P is then bounded by 2^8, exact in the end.
+constexpr float kRescaleLog2 = 8.0f;
+
+template <int D, MmaKind KIND>
+__global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTAS_PER_SM)
+    fwd_kernel(const __grid_constant__ FwdArgs a) {
+  using C = FwdCfg<D, KIND>;
+  constexpr int ST = C::STAGES;
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  __shared__ __align__(8) uint64_t bars[B_KFULL + 3 * ST];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = a.N / kTile;
+  const int BH = a.B * a.H;
+  const int lin = blockIdx.x;
+  const int qt = a.causal ? (T - 1 - lin / BH) : (lin / BH);  // longest rows first
+  const int bh = lin % BH;
+  const int b = bh / a.H, h = bh % a.H;
+  const int kvh = b * a.Hkv + h / (a.H / a.Hkv);
+  const int nkv = a.causal ? qt + 1 : T;
+
+  const uint32_t sQ = smem_u32(smem);
+  const uint32_t sKV = sQ + C::TILE_BYTES;  // stage s: K at +2s*TILE, V at +(2s+1)*TILE
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  volatile int* abort = &abort_sh;
+  unsigned int* status = a.status;
+
+  if (threadIdx.x == 0) {
+    abort_sh = 0;
+    mbar_init(bar(B_QFULL), 1);
+    mbar_init(bar(B_SFULL), 1);
+    mbar_init(bar(B_SFREE), 128);
+    mbar_init(bar(B_PFULL), 128);
+    mbar_init(bar(B_ODONE), 1);
+    mbar_init(bar(B_DRAIN), 1);
+    for (int s = 0; s < 3 * ST; ++s) mbar_init(bar(B_KFULL + s), 1);
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&a.tmQ);
+    prefetch_tmap(&a.tmK);
+    prefetch_tmap(&a.tmV);
+    prefetch_tmap(&a.tmO);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_base_sh), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int issued = 0;
+      bool ok = true;
+      mbar_expect_tx(bar(B_QFULL), C::TILE_BYTES);
+      for (int k = 0; k < C::NBLK; ++k)
+        tma_load_3d(sQ + k * C::BLK_BYTES, &a.tmQ, bar(B_QFULL), k * C::BLK_ELEMS, qt * kTile, bh);
+      for (int j = 0; j < nkv; ++j) {
+        const int s = j % ST;
+        if (j >= ST && !mbar_wait(bar(B_KFULL + 2 * ST + s), ((j / ST) - 1) & 1, abort, 1, status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sK = sKV + (2 * s) * C::TILE_BYTES, sV = sK + C::TILE_BYTES;
+        mbar_expect_tx(bar(B_KFULL + s), C::TILE_BYTES);
+        for (int k = 0; k < C::NBLK; ++k)
+          tma_load_3d(sK + k * C::BLK_BYTES, &a.tmK, bar(B_KFULL + s), k * C::BLK_ELEMS,
+                      j * kTile, kvh);
+        mbar_expect_tx(bar(B_KFULL + ST + s), C::TILE_BYTES);
+        for (int k = 0; k < C::NBLK; ++k)
+          tma_load_3d(sV + k * C::BLK_BYTES, &a.tmV, bar(B_KFULL + ST + s), k * C::BLK_ELEMS,
+                      j * kTile, kvh);
+        issued = j + 1;
+      }
+      if (!ok) {  // let the loads already issued land before the CTA exits
+        mbar_wait_drain(bar(B_QFULL), 0, 2, status);
+        for (int j = issued - ST > 0 ? issued - ST : 0; j < issued; ++j) {
+          mbar_wait_drain(bar(B_KFULL + j % ST), (j / ST) & 1, 2, status);
+          mbar_wait_drain(bar(B_KFULL + ST + j % ST), (j / ST) & 1, 2, status);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = make_idesc<KIND>(128, 128, false, false);
+      constexpr uint32_t idPV = make_idesc<KIND>(128, D, false, true);
+      auto issue_s = [&](int j) -> bool {
+        const int s = j % ST;
+        if (!mbar_wait(bar(B_KFULL + s), (j / ST) & 1, abort, 3, status)) return false;
+        tc_fence_after();
+        const uint32_t sK = sKV + (2 * s) * C::TILE_BYTES;
+#pragma unroll
+        for (int k = 0; k < C::NK_QK; ++k) {
+          const uint32_t off = ((k * 32) / 128) * C::BLK_BYTES + (k * 32) % 128;
+          mma_ss<KIND>(tmem + C::S_COL, sdesc_sw128(sQ + off, 16, 1024),
+                       sdesc_sw128(sK + off, 16, 1024), idS, k > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(B_SFULL));
+        return true;
+      };
+      bool ok = mbar_wait(bar(B_QFULL), 0, abort, 4, status) && issue_s(0);
+      for (int j = 0; ok && j < nkv; ++j) {
+        if (j + 1 < nkv) {
+          // S_{j+1} overwrites S once the softmax has read S_j.
+          if (!mbar_wait(bar(B_SFREE), j & 1, abort, 5, status) || !issue_s(j + 1)) break;
+        }
+        const int s = j % ST;
+        if (!mbar_wait(bar(B_PFULL), j & 1, abort, 6, status)) break;
+        if (!mbar_wait(bar(B_KFULL + ST + s), (j / ST) & 1, abort, 7, status)) break;
+        tc_fence_after();
+        const uint32_t sV = sKV + (2 * s + 1) * C::TILE_BYTES;
+#pragma unroll
+        for (int k = 0; k < C::NK_PV; ++k) {
+          mma_ts<KIND>(tmem + C::O_COL, tmem + C::P_COL + k * 8,
+                       sdesc_sw128(sV + k * C::KPER * 128, C::BLK_BYTES, 1024), idPV,
+                       (j > 0 || k > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(B_KFULL + 2 * ST + s));  // stage s free for the producer
+        mma_commit(bar(B_ODONE));
+      }
+      // Everything this thread issued must finish before TMEM is freed.
+      mma_commit(bar(B_DRAIN));
+      mbar_wait_drain(bar(B_DRAIN), 0, 8, status);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;  // row of the query tile == TMEM lane
+    const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const float c = a.scale * kLog2e;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      if (!mbar_wait_warp(bar(B_SFULL), j & 1, abort, 9, status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t u0[32], u1[32], u2[32], u3[32];
+      tmem_ld32(trow + C::S_COL + 0, u0);
+      tmem_ld32(trow + C::S_COL + 32, u1);
+      tmem_ld32(trow + C::S_COL + 64, u2);
+      tmem_ld32(trow + C::S_COL + 96, u3);
+      tmem_ld_wait(u0);
+      reg_fence(u1);
+      reg_fence(u2);
+      reg_fence(u3);
+      tc_fence_before();
+      mbar_arrive(bar(B_SFREE));
+      float sv[128];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        sv[i] = __uint_as_float(u0[i]);
+        sv[32 + i] = __uint_as_float(u1[i]);
+        sv[64 + i] = __uint_as_float(u2[i]);
+        sv[96 + i] = __uint_as_float(u3[i]);
+      }
+      if (a.causal && j == qt) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i > r) sv[i] = -INFINITY;
+      }
+      float mx = sv[0];
+#pragma unroll
+      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, sv[i]);
+      // PV_{j-1} must be complete before P is overwritten or O rescaled.
+      if (j > 0) {
+        if (!mbar_wait_warp(bar(B_ODONE), (j - 1) & 1, abort, 10, status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      const float m_new = fmaxf(m_ref, mx);
+      const bool need = (m_new - m_ref) * c > kRescaleLog2;  // always true on the first tile
+      float alpha = 1.f;
+      if (need) {
+        alpha = ex2((m_ref - m_new) * c);
+        m_ref = m_new;
+      }
+      const float moff = -m_ref * c;
+      float rs = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        float p[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          p[i] = ex2(fmaf(sv[32 * cc + i], c, moff));
+          rs += p[i];
+        }
+        if constexpr (KIND == MmaKind::kBF16) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(p[2 * i], p[2 * i + 1]);
+          tmem_st16(trow + C::P_COL + 16 * cc, pk);
+        } else {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pk[i] = __float_as_uint(p[i]);
+          tmem_st32(trow + C::P_COL + 32 * cc, pk);
+        }
+      }
+      l = l * alpha + rs;
+      // O rescale after P: the S registers are dead by now
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int cc = 0; cc < D; cc += 32) {
+          uint32_t o[32];
+          tmem_ld32(trow + C::O_COL + cc, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(trow + C::O_COL + cc, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(B_PFULL));
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok) ok = mbar_wait_warp(bar(B_ODONE), (nkv - 1) & 1, abort, 11, status);
+    if (ok) {
+      tc_fence_after();
+      const float inv = 1.f / l;
+      uint8_t* orow = smem + r * 128;  // Q's smem is free: every MMA is done
+#pragma unroll
+      for (int cc = 0; cc < D; cc += 32) {
+        uint32_t o[32];
+        tmem_ld32(trow + C::O_COL + cc, o);
+        tmem_ld_wait(o);
+        if constexpr (KIND == MmaKind::kBF16) {
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8) {  // 4 chunks of 8 bf16 = 16 B
+            const int col = cc + 8 * q8;
+            const int blk = col / C::BLK_ELEMS, chunk = (col % C::BLK_ELEMS) / 8;
+            uint4 v;
+            v.x = pack_bf16(__uint_as_float(o[8 * q8 + 0]) * inv, __uint_as_float(o[8 * q8 + 1]) * inv);
+            v.y = pack_bf16(__uint_as_float(o[8 * q8 + 2]) * inv, __uint_as_float(o[8 * q8 + 3]) * inv);
+            v.z = pack_bf16(__uint_as_float(o[8 * q8 + 4]) * inv, __uint_as_float(o[8 * q8 + 5]) * inv);
+            v.w = pack_bf16(__uint_as_float(o[8 * q8 + 6]) * inv, __uint_as_float(o[8 * q8 + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + blk * C::BLK_BYTES + ((chunk ^ (r & 7)) << 4)) = v;
+          }
+        } else {
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {  // 8 chunks of 4 fp32 = 16 B
+            const int col = cc + 4 * q4;
+            const int blk = col / C::BLK_ELEMS, chunk = (col % C::BLK_ELEMS) / 4;
+            uint4 v;
+            v.x = __float_as_uint(__uint_as_float(o[4 * q4 + 0]) * inv);
+            v.y = __float_as_uint(__uint_as_float(o[4 * q4 + 1]) * inv);
+            v.z = __float_as_uint(__uint_as_float(o[4 * q4 + 2]) * inv);
+            v.w = __float_as_uint(__uint_as_float(o[4 * q4 + 3]) * inv);
+            *reinterpret_cast<uint4*>(orow + blk * C::BLK_BYTES + ((chunk ^ (r & 7)) << 4)) = v;
+          }
+        }
+      }
+      a.lse[static_cast<size_t>(bh) * a.N + qt * kTile + r] = m_ref * a.scale + logf(l);
+      fence_proxy_async();
+    }
+    named_bar_sync(1, 128);
+    if (warp == 2 && lane == 0 && !*abort) {
+      for (int k = 0; k < C::NBLK; ++k)
+        tma_store_3d(&a.tmO, sQ + k * C::BLK_BYTES, k * C::BLK_ELEMS, qt * kTile, bh);
+      bulk_commit();
+      bulk_wait0();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D, MmaKind KIND>
+cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
+  using C = FwdCfg<D, KIND>;
+  auto kern = fwd_kernel<D, KIND>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = static_cast<unsigned>(a.B) * a.H * (a.N / kTile);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
+  if (a.dtype == 0 && a.d == 64) return launch_fwd_t<64, MmaKind::kBF16>(a, stream);
+  if (a.dtype == 0 && a.d == 128) return launch_fwd_t<128, MmaKind::kBF16>(a, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace nea

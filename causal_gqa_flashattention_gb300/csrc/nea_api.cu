@@ -1,0 +1,259 @@
+// nea_api.cu -- the C ABI declared in include/nea_attn.h: argument checks,
+// TMA descriptor encoding, workspace carving, launches, device status word.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/nea_attn.h"
+#include "nea_internal.h"
+
+namespace nea {
+
+// Written by kernels whose bounded waits gave up; read + cleared by
+// nea_attn_check_status().  One copy per device that loaded the library.
+__device__ unsigned int g_status_word = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+std::mutex g_mu;
+EncodeTiledFn g_encode = nullptr;
+unsigned int* g_status_ptr[kMaxDevices] = {};
+
+// Driver entry point for cuTensorMapEncodeTiled, fetched through the runtime
+// so the library needs no link-time dependency on libcuda.
+EncodeTiledFn encoder() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  return g_encode;
+}
+
+// Device address of g_status_word on the current device.
+unsigned int* status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+// 3-D view {d, N, heads} of a [heads][N][d] array, boxes of 128 B x 128 rows
+// with 128-byte swizzle (the layout the tensor-core descriptors expect).
+bool encode_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, int d, int N,
+               long long heads) {
+  EncodeTiledFn enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * esize,
+                           static_cast<cuuint64_t>(d) * esize * static_cast<cuuint64_t>(N)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esize), static_cast<cuuint32_t>(kTile), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape / option checks shared by every entry point.
+int check_common(int B, int H, int Hkv, int N, int d, float scale, int causal, int dtype) {
+  if (B < 1 || H < 1 || Hkv < 1 || N < 1 || d < 1) return NEA_ERR_INVALID;
+  if (H % Hkv != 0) return NEA_ERR_INVALID;
+  if (causal != 0 && causal != 1) return NEA_ERR_INVALID;
+  if (dtype != NEA_BF16 && dtype != NEA_F32) return NEA_ERR_INVALID;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return NEA_ERR_INVALID;
+  // Grid and TMA coordinate ranges: B*H*(N/128) CTAs, heads and rows as int.
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh > (1LL << 24) || N > (1 << 24)) return NEA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return NEA_ERR_UNSUPPORTED;
+  if (N % kTile != 0) return NEA_ERR_UNSUPPORTED;
+  if (dtype == NEA_F32) return NEA_ERR_UNSUPPORTED;
+  return NEA_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct WsLayout {
+  size_t delta, lse2, dqacc, total;
+};
+WsLayout ws_layout(int B, int H, int N, int d, int dtype) {
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  WsLayout w;
+  w.delta = 0;
+  w.lse2 = align256(rows * sizeof(float));
+  w.dqacc = w.lse2 + align256(rows * sizeof(float));
+  w.total = w.dqacc + (dtype == NEA_BF16 ? align256(rows * d * sizeof(float)) : 0);
+  return w;
+}
+
+}  // namespace
+}  // namespace nea
+
+using namespace nea;
+
+extern "C" {
+
+int nea_version(void) { return 100; }
+
+const char* nea_status_string(int status) {
+  switch (status) {
+    case NEA_OK: return "ok";
+    case NEA_ERR_INVALID: return "invalid argument";
+    case NEA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case NEA_ERR_CUDA: return "CUDA error";
+    case NEA_ERR_TIMEOUT: return "a kernel wait timed out";
+    case NEA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    default: return "unknown status";
+  }
+}
+
+int nea_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                 int Hkv, int N, int d, float scale, int causal, int dtype, void* stream) {
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
+    return NEA_ERR_INVALID;
+  int st = check_common(B, H, Hkv, N, d, scale, causal, dtype);
+  if (st != NEA_OK) return st;
+  FwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  const CUtensorMapDataType dt =
+      dtype == NEA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const int es = dtype == NEA_BF16 ? 2 : 4;
+  const long long bh = static_cast<long long>(B) * H, bkv = static_cast<long long>(B) * Hkv;
+  if (!encode_3d(&a.tmQ, Q, dt, es, d, N, bh) || !encode_3d(&a.tmK, K, dt, es, d, N, bkv) ||
+      !encode_3d(&a.tmV, V, dt, es, d, N, bkv) || !encode_3d(&a.tmO, O, dt, es, d, N, bh))
+    return NEA_ERR_CUDA;
+  a.lse = LSE;
+  a.status = status_ptr();
+  if (!a.status) return NEA_ERR_CUDA;
+  a.B = B; a.H = H; a.Hkv = Hkv; a.N = N; a.d = d; a.causal = causal;
+  a.scale = scale; a.dtype = dtype;
+  return launch_fwd(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? NEA_OK : NEA_ERR_CUDA;
+}
+
+size_t nea_attn_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d, int dtype) {
+  if (check_common(B, H, Hkv, N, d, 1.0f, 1, dtype) != NEA_OK) return 0;
+  return ws_layout(B, H, N, d, dtype).total;
+}
+
+// Shared by the backward entry points: checks and fills the arguments every
+// stage needs.  Pointers a stage does not use may be null (need_* = false).
+static int prepare_bwd(BwdArgs* a, const void* Q, const void* K, const void* V, const void* O,
+                       const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                       void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int N,
+                       int d, float scale, int causal, int dtype, bool need_io, bool need_main,
+                       bool need_maps) {
+  if (!aligned16(dQ)) return NEA_ERR_INVALID;
+  if (need_io && (!aligned16(O) || !aligned16(dO) || !aligned16(LSE))) return NEA_ERR_INVALID;
+  if (need_main && (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(dO) ||
+                    !aligned16(dK) || !aligned16(dV)))
+    return NEA_ERR_INVALID;
+  int st = check_common(B, H, Hkv, N, d, scale, causal, dtype);
+  if (st != NEA_OK) return st;
+  const WsLayout w = ws_layout(B, H, N, d, dtype);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < w.total)
+    return NEA_ERR_WORKSPACE;
+  std::memset(a, 0, sizeof(*a));
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a->delta = reinterpret_cast<float*>(ws + w.delta);
+  a->lse2 = reinterpret_cast<float*>(ws + w.lse2);
+  a->dq_acc = dtype == NEA_BF16 ? reinterpret_cast<float*>(ws + w.dqacc) : static_cast<float*>(dQ);
+  if (need_maps) {
+    const CUtensorMapDataType dt =
+        dtype == NEA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const int es = dtype == NEA_BF16 ? 2 : 4;
+    const long long bh = static_cast<long long>(B) * H, bkv = static_cast<long long>(B) * Hkv;
+    if (!encode_3d(&a->tmQ, Q, dt, es, d, N, bh) || !encode_3d(&a->tmK, K, dt, es, d, N, bkv) ||
+        !encode_3d(&a->tmV, V, dt, es, d, N, bkv) || !encode_3d(&a->tmdO, dO, dt, es, d, N, bh) ||
+        !encode_3d(&a->tmdQacc, a->dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, N, bh))
+      return NEA_ERR_CUDA;
+    a->status = status_ptr();
+    if (!a->status) return NEA_ERR_CUDA;
+  }
+  a->O = O; a->dO = dO; a->lse = LSE; a->dQ = dQ; a->dK = dK; a->dV = dV;
+  a->B = B; a->H = H; a->Hkv = Hkv; a->N = N; a->d = d; a->causal = causal;
+  a->scale = scale; a->dtype = dtype;
+  return NEA_OK;
+}
+
+int nea_attn_bwd_preprocess(const void* O, const void* dO, const float* LSE, void* dQ,
+                            void* workspace, size_t workspace_bytes, int B, int H, int Hkv,
+                            int N, int d, float scale, int dtype, void* stream) {
+  BwdArgs a;
+  int st = prepare_bwd(&a, nullptr, nullptr, nullptr, O, dO, LSE, dQ, nullptr, nullptr, workspace,
+                       workspace_bytes, B, H, Hkv, N, d, scale, 1, dtype, true, false, false);
+  if (st != NEA_OK) return st;
+  return launch_bwd_pre(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? NEA_OK
+                                                                             : NEA_ERR_CUDA;
+}
+
+int nea_attn_bwd_main(const void* Q, const void* K, const void* V, const void* dO, void* dQ,
+                      void* dK, void* dV, void* workspace, size_t workspace_bytes, int B, int H,
+                      int Hkv, int N, int d, float scale, int causal, int dtype, void* stream) {
+  BwdArgs a;
+  int st = prepare_bwd(&a, Q, K, V, nullptr, dO, nullptr, dQ, dK, dV, workspace, workspace_bytes,
+                       B, H, Hkv, N, d, scale, causal, dtype, false, true, true);
+  if (st != NEA_OK) return st;
+  return launch_bwd_main(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? NEA_OK
+                                                                              : NEA_ERR_CUDA;
+}
+
+int nea_attn_bwd_finalize(void* dQ, void* workspace, size_t workspace_bytes, int B, int H,
+                          int Hkv, int N, int d, int dtype, void* stream) {
+  BwdArgs a;
+  int st = prepare_bwd(&a, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, dQ, nullptr,
+                       nullptr, workspace, workspace_bytes, B, H, Hkv, N, d, 1.0f, 1, dtype,
+                       false, false, false);
+  if (st != NEA_OK) return st;
+  if (dtype != NEA_BF16) return NEA_OK;
+  return launch_bwd_post(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? NEA_OK
+                                                                              : NEA_ERR_CUDA;
+}
+
+int nea_attn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                 const float* LSE, void* dQ, void* dK, void* dV, void* workspace,
+                 size_t workspace_bytes, int B, int H, int Hkv, int N, int d, float scale,
+                 int causal, int dtype, void* stream) {
+  BwdArgs a;
+  int st = prepare_bwd(&a, Q, K, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes, B, H, Hkv,
+                       N, d, scale, causal, dtype, true, true, true);
+  if (st != NEA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_bwd_pre(a, s) != cudaSuccess) return NEA_ERR_CUDA;
+  if (launch_bwd_main(a, s) != cudaSuccess) return NEA_ERR_CUDA;
+  if (dtype == NEA_BF16 && launch_bwd_post(a, s) != cudaSuccess) return NEA_ERR_CUDA;
+  return NEA_OK;
+}
+
+int nea_attn_check_status(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return NEA_ERR_CUDA;
+  unsigned int word = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&word, g_status_word, sizeof(word)) != cudaSuccess) return NEA_ERR_CUDA;
+  if (word != 0 && cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess)
+    return NEA_ERR_CUDA;
+  return word != 0 ? NEA_ERR_TIMEOUT : NEA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,48 @@
+// nea_internal.h -- launcher interface between the C-ABI translation unit
+// (nea_api.cu) and the kernel translation units.  Not installed.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace nea {
+
+// Tiles are 128 query rows x 128 key rows for every kernel.
+constexpr int kTile = 128;
+
+struct FwdArgs {
+  CUtensorMap tmQ, tmK, tmV, tmO;  // 3-D maps {d, N, heads}, 128-B swizzle
+  float* lse;                      // [B*H*N]
+  unsigned int* status;            // device status word
+  int B, H, Hkv, N, d, causal;
+  float scale;                     // softmax scale
+  int dtype;                       // 0 bf16, 1 fp32
+};
+
+struct BwdArgs {
+  CUtensorMap tmQ, tmK, tmV, tmdO;  // loads, 3-D {d, N, heads}, 128-B swizzle
+  CUtensorMap tmdQacc;              // fp32 reduce target {d, N, B*H}, 128-B swizzle
+  const void* O;                    // [B,H,N,d] dtype
+  const void* dO;
+  const float* lse;                 // [B*H*N]
+  float* delta;                     // workspace: D [B*H*N]
+  float* lse2;                      // workspace: LSE * log2(e) [B*H*N]
+  float* dq_acc;                    // fp32 dQ accumulator [B,H,N,d] (== dQ for fp32)
+  void* dQ;                         // output
+  void* dK;
+  void* dV;
+  unsigned int* status;
+  int B, H, Hkv, N, d, causal;
+  float scale;
+  int dtype;
+};
+
+// Each launcher validates nothing (the API layer did) and returns the
+// cudaError_t of its launch(es).
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_post(const BwdArgs& a, cudaStream_t stream);
+
+}  // namespace nea

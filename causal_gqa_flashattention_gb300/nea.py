@@ -1,0 +1,182 @@
+"""ctypes binding of ``libnea_attn.so`` (the C ABI of include/nea_attn.h).
+
+Argument marshalling only: every step of the attention runs in the library's
+CUDA kernels.  PyTorch provides device memory (output tensors are allocated
+with ``torch.empty`` when the caller passes none) and the current stream.
+There is no fallback: if the library is missing or a call fails, this module
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libnea_attn.so")
+
+NEA_OK = 0
+NEA_ERR_INVALID = -1
+NEA_ERR_UNSUPPORTED = -2
+NEA_ERR_CUDA = -3
+NEA_ERR_TIMEOUT = -4
+NEA_ERR_WORKSPACE = -5
+NEA_BF16 = 0
+NEA_F32 = 1
+
+_lock = threading.Lock()
+_lib = None
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_f = ctypes.c_float
+
+
+class NeaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+def lib():
+    """Load the library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                                   "`python -c 'import __graft_entry__ as g; g.build()'`")
+            L = ctypes.CDLL(LIB_PATH)
+            L.nea_attn_fwd.argtypes = [_vp] * 5 + [_i] * 5 + [_f, _i, _i, _vp]
+            L.nea_attn_fwd.restype = _i
+            L.nea_attn_bwd_workspace_bytes.argtypes = [_i] * 6
+            L.nea_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+            L.nea_attn_bwd.argtypes = [_vp] * 10 + [ctypes.c_size_t] + [_i] * 5 + [_f, _i, _i, _vp]
+            L.nea_attn_bwd.restype = _i
+            L.nea_attn_bwd_preprocess.argtypes = [_vp] * 5 + [ctypes.c_size_t] + [_i] * 5 + [
+                _f, _i, _vp]
+            L.nea_attn_bwd_preprocess.restype = _i
+            L.nea_attn_bwd_main.argtypes = [_vp] * 8 + [ctypes.c_size_t] + [_i] * 5 + [
+                _f, _i, _i, _vp]
+            L.nea_attn_bwd_main.restype = _i
+            L.nea_attn_bwd_finalize.argtypes = [_vp] * 2 + [ctypes.c_size_t] + [_i] * 6 + [_vp]
+            L.nea_attn_bwd_finalize.restype = _i
+            L.nea_attn_check_status.argtypes = [_vp]
+            L.nea_attn_check_status.restype = _i
+            L.nea_status_string.argtypes = [_i]
+            L.nea_status_string.restype = ctypes.c_char_p
+            L.nea_version.restype = _i
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().nea_status_string(int(status)).decode()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return NEA_BF16
+    if t.dtype == torch.float32:
+        return NEA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _check(q, k, v):
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA tensors")
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (B, Hkv, N, d) or v.shape != k.shape:
+        raise ValueError("k / v must be [B, Hkv, N, d]")
+    return B, H, Hkv, N, d
+
+
+def attn_fwd(q, k, v, *, causal=True, scale=None, out=None, lse=None, stream=None):
+    """O, LSE = attention(q, k, v).  q [B,H,N,d], k/v [B,Hkv,N,d] (bf16)."""
+    B, H, Hkv, N, d = _check(q, k, v)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    lse_t = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    st = lib().nea_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse_t), B, H, Hkv, N, d,
+                            scale, int(bool(causal)), _dtype_code(q),
+                            ctypes.c_void_p(_stream_handle(stream)))
+    if st != NEA_OK:
+        raise NeaError(st, "nea_attn_fwd")
+    return o, lse_t
+
+
+def bwd_workspace_bytes(B, H, Hkv, N, d, dtype=NEA_BF16) -> int:
+    return int(lib().nea_attn_bwd_workspace_bytes(B, H, Hkv, N, d, dtype))
+
+
+def attn_bwd(q, k, v, o, do, lse, *, causal=True, scale=None, dq=None, dk=None, dv=None,
+             workspace=None, stream=None):
+    """dQ, dK, dV for upstream gradient ``do``, using the forward's O and LSE."""
+    B, H, Hkv, N, d = _check(q, k, v)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    code = _dtype_code(q)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = bwd_workspace_bytes(B, H, Hkv, N, d, code)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = lib().nea_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                            _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(), B, H, Hkv, N,
+                            d, scale, int(bool(causal)), code,
+                            ctypes.c_void_p(_stream_handle(stream)))
+    if st != NEA_OK:
+        raise NeaError(st, "nea_attn_bwd")
+    return dq, dk, dv
+
+
+def attn_bwd_stages(q, k, v, o, do, lse, dq, dk, dv, workspace, *, causal=True, scale=None,
+                    stream=None, between=None):
+    """The backward as its three ABI stages (same work as ``attn_bwd``).
+    ``between(i)`` is called before stage i (0, 1, 2) and after the last
+    (i = 3), e.g. to record CUDA events between the kernels."""
+    B, H, Hkv, N, d = _check(q, k, v)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    code = _dtype_code(q)
+    s = ctypes.c_void_p(_stream_handle(stream))
+    L = lib()
+    nb = workspace.numel()
+    if between:
+        between(0)
+    st = L.nea_attn_bwd_preprocess(_ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(workspace), nb,
+                                   B, H, Hkv, N, d, scale, code, s)
+    if st != NEA_OK:
+        raise NeaError(st, "nea_attn_bwd_preprocess")
+    if between:
+        between(1)
+    st = L.nea_attn_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
+                             _ptr(workspace), nb, B, H, Hkv, N, d, scale, int(bool(causal)), code,
+                             s)
+    if st != NEA_OK:
+        raise NeaError(st, "nea_attn_bwd_main")
+    if between:
+        between(2)
+    st = L.nea_attn_bwd_finalize(_ptr(dq), _ptr(workspace), nb, B, H, Hkv, N, d, code, s)
+    if st != NEA_OK:
+        raise NeaError(st, "nea_attn_bwd_finalize")
+    if between:
+        between(3)
+    return dq, dk, dv
+
+
+def check_status(stream=None) -> int:
+    return int(lib().nea_attn_check_status(ctypes.c_void_p(_stream_handle(stream))))

@@ -1,0 +1,146 @@
+/*
+ * nea_attn.h -- C ABI of the causal grouped-query FlashAttention library
+ * (forward and backward) for GB300 / sm_103a.
+ *
+ * What it computes.  Softmax attention with a causal mask and grouped-query
+ * heads, and its gradient:
+ *   "NanoEuler: Hand-writing GPT-2 in Pure C/CUDA", section "Tiled
+ *   FlashAttention" -- attention computed tile by tile with an online
+ *   softmax, so that no N x N matrix reaches global memory;
+ *   same post, "Architecture Deep Dive" -- a GPT-2 style decoder, so row i
+ *   attends keys j <= i;
+ *   same post, "Build and Run" (config file: num_heads 12, num_kv_heads 4)
+ *   -- grouped-query attention; query head h reads KV head h / (H / Hkv);
+ *   same post, "Hand-written Backpropagation" -- a hand-derived backward.
+ *
+ *   S_ij = scale * Q_i . K_j          P = softmax_j(S) (j <= i when causal)
+ *   O_i  = sum_j P_ij V_j             LSE_i = ln sum_j exp(S_ij)
+ *   dP_ij = dO_i . V_j   D_i = dO_i . O_i   dS_ij = P_ij (dP_ij - D_i)
+ *   dQ_i = scale sum_j dS_ij K_j
+ *   dK_j = scale sum_{h in group} sum_i dS_ij Q_i
+ *   dV_j =       sum_{h in group} sum_i P_ij dO_i
+ *
+ * Conventions shared by every entry point.
+ *   Pointers are DEVICE pointers (from cudaMalloc or any allocator of the
+ *   current device), 16-byte aligned, to contiguous row-major arrays:
+ *     Q, O, dO, dQ : [B][H][N][d]        K, V, dK, dV : [B][Hkv][N][d]
+ *     LSE          : [B][H][N] float32, natural log of the scaled logits
+ *   Element type of Q/K/V/O/dO/dQ/dK/dV is `dtype` (bf16 or fp32); all
+ *   accumulation is fp32; bf16 path: P and dS enter the tensor cores as
+ *   bf16; fp32 path: operands enter as TF32.
+ *   Supported: d in {64, 128} for bf16, d = 64 for fp32; H % Hkv == 0;
+ *   N >= 1 and N % 128 == 0 (ragged N returns NEA_ERR_UNSUPPORTED);
+ *   causal in {0, 1}; scale finite and > 0; B >= 1.
+ *   `stream` is a cudaStream_t (NULL = legacy default stream).
+ *   The caller owns every buffer.  No entry point allocates device memory.
+ *   Calls validate their arguments on the host and return a status code
+ *   synchronously; kernels then run asynchronously on `stream`.  Errors met
+ *   while the kernels run are reported by nea_attn_check_status().  Outputs
+ *   are unspecified when the status is not NEA_OK.
+ *   Not thread-safe with respect to nea_attn_check_status() on the same
+ *   device: the device status word is shared by all calls of the process.
+ */
+#ifndef NEA_ATTN_H_
+#define NEA_ATTN_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  NEA_OK = 0,
+  NEA_ERR_INVALID = -1,     /* bad argument: null / misaligned pointer, bad size */
+  NEA_ERR_UNSUPPORTED = -2, /* valid but not implemented (d, dtype, ragged N) */
+  NEA_ERR_CUDA = -3,        /* a CUDA runtime / driver call failed */
+  NEA_ERR_TIMEOUT = -4,     /* a kernel's bounded wait gave up (see check_status) */
+  NEA_ERR_WORKSPACE = -5    /* workspace null, misaligned or too small */
+} nea_status;
+
+typedef enum { NEA_BF16 = 0, NEA_F32 = 1 } nea_dtype;
+
+/*
+ * Forward.  Writes O [B,H,N,d] (dtype) and LSE [B,H,N] (fp32, natural log).
+ * Section "Tiled FlashAttention": one CTA per 128-row query tile of one
+ * (batch, head); K/V tiles of 128 rows stream through shared memory; tiles
+ * entirely above the causal diagonal are skipped.
+ */
+int nea_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                 int Hkv, int N, int d, float scale, int causal, int dtype, void* stream);
+
+/*
+ * Bytes of device workspace nea_attn_bwd() needs for these sizes (256-byte
+ * aligned sub-buffers: D [B,H,N] fp32, LSE*log2(e) [B,H,N] fp32 and, for
+ * bf16, the fp32 dQ accumulator [B,H,N,d]).  Returns 0 for invalid sizes.
+ */
+size_t nea_attn_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d, int dtype);
+
+/*
+ * Backward.  Given the forward's inputs, its O and LSE, and the upstream
+ * gradient dO, writes dQ [B,H,N,d], dK and dV [B,Hkv,N,d] (dtype).
+ * Section "Hand-written Backpropagation": the gradient is derived by hand
+ * and P is recomputed from LSE instead of stored.  Three kernels run in
+ * order on `stream`: a preprocess D = rowsum(dO * O) (which also clears the
+ * dQ accumulator), the main kernel (one CTA per 128-row KV tile of one
+ * (batch, KV head); dK and dV are summed over the group's query heads in
+ * tensor memory, without atomics; dQ partials are added into the fp32
+ * accumulator by TMA reductions), and, for bf16, a cast of dQ.
+ * `workspace` is a device buffer of at least
+ * nea_attn_bwd_workspace_bytes(...) bytes, 256-byte aligned, owned by the
+ * caller and not used concurrently by another call; its contents on entry
+ * do not matter.  The order of the dQ additions is not fixed, so dQ may
+ * differ between runs in the last bits; dK and dV are deterministic.
+ */
+int nea_attn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                 const float* LSE, void* dQ, void* dK, void* dV, void* workspace,
+                 size_t workspace_bytes, int B, int H, int Hkv, int N, int d, float scale,
+                 int causal, int dtype, void* stream);
+
+/*
+ * The three stages nea_attn_bwd() runs, exposed so that a caller can place
+ * events between them (profiling) or overlap them with its own work.  Called
+ * in this order on one stream, with one workspace, they are exactly
+ * nea_attn_bwd().  Arguments mean the same as there.
+ *
+ * Stage 1, preprocess (HBM-bound): writes scale * rowsum(dO * O) and
+ * LSE * log2(e) per row into the workspace and clears the fp32 dQ
+ * accumulator (for fp32 dtype the accumulator is dQ itself).
+ */
+int nea_attn_bwd_preprocess(const void* O, const void* dO, const float* LSE, void* dQ,
+                            void* workspace, size_t workspace_bytes, int B, int H, int Hkv,
+                            int N, int d, float scale, int dtype, void* stream);
+
+/*
+ * Stage 2, main kernel: reads Q, K, V, dO and the stage-1 workspace; writes
+ * dK, dV and adds every dQ partial into the accumulator.
+ */
+int nea_attn_bwd_main(const void* Q, const void* K, const void* V, const void* dO, void* dQ,
+                      void* dK, void* dV, void* workspace, size_t workspace_bytes, int B, int H,
+                      int Hkv, int N, int d, float scale, int causal, int dtype, void* stream);
+
+/*
+ * Stage 3, finalize: dQ = bf16(accumulator) for bf16; nothing to do (and
+ * NEA_OK) for fp32.
+ */
+int nea_attn_bwd_finalize(void* dQ, void* workspace, size_t workspace_bytes, int B, int H,
+                          int Hkv, int N, int d, int dtype, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device status
+ * word.  Returns NEA_ERR_TIMEOUT if a kernel's bounded wait gave up since
+ * the last check, NEA_ERR_CUDA if the stream reports an error, else NEA_OK.
+ */
+int nea_attn_check_status(void* stream);
+
+/* Static, human-readable text for a status code. */
+const char* nea_status_string(int status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int nea_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NEA_ATTN_H_ */

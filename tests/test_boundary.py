@@ -1,0 +1,105 @@
+"""Host-side checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments with the documented status codes
+before touching the GPU (every call below fails validation, so none launches)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nea_attn.h")
+
+
+@pytest.fixture(scope="module")
+def nea():
+    from causal_gqa_flashattention_gb300 import build, nea as binding
+    build.build()
+    binding.lib()
+    return binding
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(nea_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("nea_attn_fwd", "nea_attn_bwd", "nea_attn_bwd_workspace_bytes",
+              "nea_attn_check_status", "nea_status_string", "nea_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(nea):
+    L = nea.lib()
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(nea):
+    for code in (0, -1, -2, -3, -4, -5):
+        assert nea.status_string(code) not in ("", "unknown status")
+    assert nea.status_string(7) == "unknown status"
+    assert nea.lib().nea_version() >= 100
+
+
+GOOD = dict(B=2, H=12, Hkv=4, N=1024, d=64, scale=0.125, causal=1, dtype=0)
+P = 1 << 20  # a 16-byte aligned fake address: validation fails before any use
+
+
+def fwd(nea, ptrs=None, **kw):
+    a = dict(GOOD, **kw)
+    ptrs = ptrs or [P] * 5
+    return nea.lib().nea_attn_fwd(*[ctypes.c_void_p(p) for p in ptrs], a["B"], a["H"], a["Hkv"],
+                                  a["N"], a["d"], a["scale"], a["causal"], a["dtype"], None)
+
+
+def bwd(nea, ptrs=None, ws=P, ws_bytes=1 << 40, **kw):
+    a = dict(GOOD, **kw)
+    ptrs = ptrs or [P] * 9
+    return nea.lib().nea_attn_bwd(*[ctypes.c_void_p(p) for p in ptrs], ctypes.c_void_p(ws),
+                                  ws_bytes, a["B"], a["H"], a["Hkv"], a["N"], a["d"], a["scale"],
+                                  a["causal"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(H=12, Hkv=5), -1), (dict(B=0), -1), (dict(N=0), -1), (dict(d=0), -1),
+    (dict(causal=2), -1), (dict(dtype=3), -1), (dict(scale=0.0), -1),
+    (dict(scale=float("nan")), -1), (dict(scale=float("inf")), -1), (dict(scale=-1.0), -1),
+    (dict(d=96), -2), (dict(d=32), -2), (dict(N=1000), -2), (dict(N=100), -2),
+    (dict(dtype=1), -2),
+])
+def test_invalid_and_unsupported_arguments(nea, kw, code):
+    assert fwd(nea, **kw) == code
+    assert bwd(nea, **kw) == code
+
+
+@pytest.mark.parametrize("which", range(5))
+def test_null_and_misaligned_pointers_fwd(nea, which):
+    ptrs = [P] * 5
+    ptrs[which] = 0
+    assert fwd(nea, ptrs) == -1
+    ptrs[which] = P + 8
+    assert fwd(nea, ptrs) == -1
+
+
+@pytest.mark.parametrize("which", range(9))
+def test_null_and_misaligned_pointers_bwd(nea, which):
+    ptrs = [P] * 9
+    ptrs[which] = 0
+    assert bwd(nea, ptrs) == -1
+    ptrs[which] = P + 4
+    assert bwd(nea, ptrs) == -1
+
+
+def test_workspace_checks(nea):
+    need = nea.bwd_workspace_bytes(2, 12, 4, 1024, 64, 0)
+    rows = 2 * 12 * 1024
+    assert need >= rows * 4 * 2 + rows * 64 * 4
+    assert bwd(nea, ws=0) == -5
+    assert bwd(nea, ws=P + 16) == -5          # not 256-byte aligned
+    assert bwd(nea, ws_bytes=need - 1) == -5
+    assert nea.bwd_workspace_bytes(2, 12, 5, 1024, 64, 0) == 0
+    assert nea.bwd_workspace_bytes(2, 12, 4, 1000, 64, 0) == 0

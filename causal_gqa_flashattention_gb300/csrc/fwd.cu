@@ -41,9 +41,14 @@ struct FwdCfg {
   static constexpr int TMEM_COLS = pow2_cols(P_COL + P_COLS);
   static constexpr int CTAS_PER_SM = TMEM_COLS <= 256 ? 2 : 1;
   static constexpr int STAGES = 2;
-  static constexpr int THREADS = 192;
-  // Q tile, then per stage: K tile, V tile.  +1 KB for 1024-B alignment.
-  static constexpr int SMEM_BYTES = 1024 + TILE_BYTES * (1 + 2 * STAGES);
+  // tf32 operands must be K-major, so for tf32 a transposer warpgroup
+  // (warps 6..9) rewrites each V tile as V^T [d][keys] before O += P V^T^T.
+  static constexpr bool TRANSPOSE_V = KIND == MmaKind::kTF32;
+  static constexpr int THREADS = TRANSPOSE_V ? 320 : 192;
+  static constexpr int VT_BYTES = TRANSPOSE_V ? TILE_BYTES : 0;
+  static constexpr int VT_BLK_BYTES = D * 128;  // one 32-key column block of V^T
+  // Q tile, then per stage: K tile, V tile (, V^T).  +1 KB for alignment.
+  static constexpr int SMEM_BYTES = 1024 + TILE_BYTES * (1 + 2 * STAGES) + VT_BYTES * STAGES;
 };
 
 // mbarrier slots
@@ -63,7 +68,7 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  __shared__ __align__(8) uint64_t bars[B_KFULL + 3 * ST];
+  __shared__ __align__(8) uint64_t bars[B_KFULL + 4 * ST];  // + VT_FULL[s] = B_KFULL + 3 ST + s
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -79,6 +84,7 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
 
   const uint32_t sQ = smem_u32(smem);
   const uint32_t sKV = sQ + C::TILE_BYTES;  // stage s: K at +2s*TILE, V at +(2s+1)*TILE
+  const uint32_t sVT = sKV + 2 * ST * C::TILE_BYTES;  // stage s: V^T at +s*VT_BYTES
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   volatile int* abort = &abort_sh;
   unsigned int* status = a.status;
@@ -92,6 +98,7 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
     mbar_init(bar(B_ODONE), 1);
     mbar_init(bar(B_DRAIN), 1);
     for (int s = 0; s < 3 * ST; ++s) mbar_init(bar(B_KFULL + s), 1);
+    for (int s = 0; s < ST; ++s) mbar_init(bar(B_KFULL + 3 * ST + s), 128);
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -146,7 +153,7 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idS = make_idesc<KIND>(128, 128, false, false);
-      constexpr uint32_t idPV = make_idesc<KIND>(128, D, false, true);
+      constexpr uint32_t idPV = make_idesc<KIND>(128, D, false, !C::TRANSPOSE_V);
       auto issue_s = [&](int j) -> bool {
         const int s = j % ST;
         if (!mbar_wait(bar(B_KFULL + s), (j / ST) & 1, abort, 3, status)) return false;
@@ -169,13 +176,19 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
         }
         const int s = j % ST;
         if (!mbar_wait(bar(B_PFULL), j & 1, abort, 6, status)) break;
-        if (!mbar_wait(bar(B_KFULL + ST + s), (j / ST) & 1, abort, 7, status)) break;
+        const int vbar = C::TRANSPOSE_V ? B_KFULL + 3 * ST + s : B_KFULL + ST + s;
+        if (!mbar_wait(bar(vbar), (j / ST) & 1, abort, 7, status)) break;
         tc_fence_after();
         const uint32_t sV = sKV + (2 * s + 1) * C::TILE_BYTES;
 #pragma unroll
         for (int k = 0; k < C::NK_PV; ++k) {
-          mma_ts<KIND>(tmem + C::O_COL, tmem + C::P_COL + k * 8,
-                       sdesc_sw128(sV + k * C::KPER * 128, C::BLK_BYTES, 1024), idPV,
+          uint64_t bdesc;
+          if constexpr (C::TRANSPOSE_V)  // V^T K-major: 32-B K-step, 4 per 128-B block
+            bdesc = sdesc_sw128(sVT + s * C::VT_BYTES + (k / 4) * C::VT_BLK_BYTES + (k % 4) * 32,
+                                16, 1024);
+          else  // V MN-major: K-step = KPER rows of 128 B
+            bdesc = sdesc_sw128(sV + k * C::KPER * 128, C::BLK_BYTES, 1024);
+          mma_ts<KIND>(tmem + C::O_COL, tmem + C::P_COL + k * 8, bdesc, idPV,
                        (j > 0 || k > 0) ? 1u : 0u);
         }
         mma_commit(bar(B_KFULL + 2 * ST + s));  // stage s free for the producer
@@ -184,6 +197,35 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
       // Everything this thread issued must finish before TMEM is freed.
       mma_commit(bar(B_DRAIN));
       mbar_wait_drain(bar(B_DRAIN), 0, 8, status);
+    }
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ V transposer
+    // (tf32 only) thread t = key row t of V_j; writes column t of V^T.
+    if constexpr (C::TRANSPOSE_V) {
+      const int t = threadIdx.x - 192;
+      for (int j = 0; j < nkv; ++j) {
+        const int s = j % ST;
+        if (!mbar_wait_warp(bar(B_KFULL + ST + s), (j / ST) & 1, abort, 12, status)) break;
+        const uint8_t* vrow = smem + (sKV - sQ) + (2 * s + 1) * C::TILE_BYTES + t * 128;
+        uint8_t* vt = smem + (sVT - sQ) + s * C::VT_BYTES + (t / 32) * C::VT_BLK_BYTES + (t % 4) * 4;
+        const int tchunk = (t % 32) / 4;
+#pragma unroll
+        for (int blk = 0; blk < C::NBLK; ++blk) {
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            const float4 x =
+                *reinterpret_cast<const float4*>(vrow + blk * C::BLK_BYTES + ((ch ^ (t & 7)) << 4));
+            const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int c = blk * 32 + ch * 4 + e;  // column of V = row of V^T
+              *reinterpret_cast<float*>(vt + c * 128 + ((tchunk ^ (c & 7)) << 4)) = xs[e];
+            }
+          }
+        }
+        fence_proxy_async();
+        mbar_arrive(bar(B_KFULL + 3 * ST + s));
+      }
     }
   } else {
     // ------------------------------------------------------------ softmax
@@ -354,6 +396,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
   if (a.dtype == 0 && a.d == 64) return launch_fwd_t<64, MmaKind::kBF16>(a, stream);
   if (a.dtype == 0 && a.d == 128) return launch_fwd_t<128, MmaKind::kBF16>(a, stream);
+  if (a.dtype == 1 && a.d == 64) return launch_fwd_t<64, MmaKind::kTF32>(a, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -76,8 +76,10 @@ bool encode_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esi
 
 bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Shape / option checks shared by every entry point.
-int check_common(int B, int H, int Hkv, int N, int d, float scale, int causal, int dtype) {
+// Shape / option checks shared by every entry point.  `bwd`: the checks of
+// the backward, which supports fewer fp32 shapes than the forward.
+int check_common(int B, int H, int Hkv, int N, int d, float scale, int causal, int dtype,
+                 bool bwd = true) {
   if (B < 1 || H < 1 || Hkv < 1 || N < 1 || d < 1) return NEA_ERR_INVALID;
   if (H % Hkv != 0) return NEA_ERR_INVALID;
   if (causal != 0 && causal != 1) return NEA_ERR_INVALID;
@@ -88,7 +90,7 @@ int check_common(int B, int H, int Hkv, int N, int d, float scale, int causal, i
   if (bh > (1LL << 24) || N > (1 << 24)) return NEA_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return NEA_ERR_UNSUPPORTED;
   if (N % kTile != 0) return NEA_ERR_UNSUPPORTED;
-  if (dtype == NEA_F32) return NEA_ERR_UNSUPPORTED;
+  if (dtype == NEA_F32 && (bwd || d != 64)) return NEA_ERR_UNSUPPORTED;
   return NEA_OK;
 }
 
@@ -132,7 +134,7 @@ int nea_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LS
                  int Hkv, int N, int d, float scale, int causal, int dtype, void* stream) {
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
     return NEA_ERR_INVALID;
-  int st = check_common(B, H, Hkv, N, d, scale, causal, dtype);
+  int st = check_common(B, H, Hkv, N, d, scale, causal, dtype, /*bwd=*/false);
   if (st != NEA_OK) return st;
   FwdArgs a;
   std::memset(&a, 0, sizeof(a));

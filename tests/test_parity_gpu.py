@@ -17,6 +17,7 @@ pytestmark = pytest.mark.gpu
 O_MAXABS = 2e-2
 LSE_MAXABS = 1e-3
 GRAD_REL = 1e-2
+F32_REL = 5e-3
 
 
 @pytest.fixture(scope="module")
@@ -54,7 +55,10 @@ def run_case(nea, w, seed=0, check_bwd=True):
     ro, rlse = oracle.attn_fwd(qc, kc, vc, w.scale, w.causal)
     assert finite(o, lse)
     e_o, e_lse = maxabs(o, ro), maxabs(lse, rlse)
-    assert e_o <= O_MAXABS, e_o
+    if w.dtype == "bf16":
+        assert e_o <= O_MAXABS, e_o
+    else:  # fp32 inputs, TF32 tensor-core operands
+        assert rel_l2(o, ro) <= F32_REL, rel_l2(o, ro)
     assert e_lse <= LSE_MAXABS, e_lse
     if not check_bwd:
         return
@@ -105,3 +109,10 @@ def test_second_seed_and_repeat(nea):
 @pytest.mark.parametrize("name", ["gpt2s_bf16", "long_bf16", "wide_bf16"])
 def test_full_size_workloads(nea, name):
     run_case(nea, WORKLOADS[name])
+
+
+@pytest.mark.parametrize("w", [WORKLOADS["tiny_f32"], custom(2, 6, 2, 384, 64, "f32"),
+                               custom(1, 4, 2, 256, 64, "f32", causal=False),
+                               WORKLOADS["gpt2s_f32"]], ids=lambda w: w.name)
+def test_f32_forward(nea, w):
+    run_case(nea, w, check_bwd=False)

@@ -127,6 +127,34 @@ int nea_attn_bwd_finalize(void* dQ, void* workspace, size_t workspace_bytes, int
                           int Hkv, int N, int d, int dtype, void* stream);
 
 /*
+ * Backward without a caller workspace.  The pages have no counterpart: this
+ * entry point exists for callers that cannot allocate device memory -- a
+ * host framework that hands a plugin only its input and output pointers, or
+ * a path on which cudaMalloc (which can synchronise the whole device) is not
+ * allowed.  Same arguments and results as nea_attn_bwd() minus the
+ * workspace; the scratch (D, LSE*log2(e) and the fp32 dQ accumulator) lives
+ * in a fixed array of nea_attn_bwd_noalloc_max_bytes() bytes (32 MiB) inside
+ * the library, reserved on every GPU that loads it until the process exits.
+ *   - Sizes whose nea_attn_bwd_workspace_bytes() exceeds that maximum return
+ *     NEA_ERR_WORKSPACE and launch nothing.
+ *   - No cudaMalloc, cudaFree or other allocating call is made.  The first
+ *     call on a device looks up the array's device address there
+ *     (cudaGetSymbolAddress) and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call uses the same array, and each call rewrites all of it that
+ *     it reads (the dQ accumulator is cleared by the preprocess kernel), so
+ *     sequential calls are independent.  Calls that overlap on the GPU (other
+ *     streams, other host threads) race on the array: serialise them.
+ */
+int nea_attn_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
+                         const void* dO, const float* LSE, void* dQ, void* dK, void* dV, int B,
+                         int H, int Hkv, int N, int d, float scale, int causal, int dtype,
+                         void* stream);
+
+/* Size in bytes of the scratch array behind nea_attn_bwd_noalloc(). */
+size_t nea_attn_bwd_noalloc_max_bytes(void);
+
+/*
  * Synchronises `stream`, then reads and clears the library's device status
  * word.  Returns NEA_ERR_TIMEOUT if a kernel's bounded wait gave up since
  * the last check, NEA_ERR_CUDA if the stream reports an error, else NEA_OK.

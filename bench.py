@@ -70,54 +70,103 @@ def traffic_for(kernel):
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """Samples SM clock and clock-event (throttle) reasons while the timed
+    region runs: NVML polled from a thread every ~1 ms (the region is a few
+    milliseconds long), falling back to `nvidia-smi -lms 100`.  Read-only."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, index):
-        self.index = index
-        self.proc = None
+    def __init__(self, device_index):
+        self.device_index = device_index
+        self.samples, self.max_mhz, self.reasons = [], None, set()
+        self.proc, self.thread, self.stop = None, None, False
+        self.source = "none"
+
+    def _nvml(self):
+        import ctypes
+        import torch
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        props = torch.cuda.get_device_properties(self.device_index)
+        bus = None
+        if hasattr(props, "pci_bus_id"):
+            bus = "%08x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id,
+                                        getattr(props, "pci_device_id", 0))
+        if bus is None or lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)):
+            if lib.nvmlDeviceGetHandleByIndex_v2(self.device_index, ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle")
+        getr = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+        return lib, h, getr
 
     def __enter__(self):
+        import ctypes
+        import threading
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
+            lib, h, getr = self._nvml()
+            self.source = "nvml"
+
+            def run():
+                clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+                while not self.stop:
+                    if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                        self.samples.append(float(clk.value))
+                    if getr(h, ctypes.byref(rs)) == 0:
+                        for bit, name in self.REASONS.items():
+                            if rs.value & bit:
+                                self.reasons.add(name)
+                    time.sleep(0.001)
+            self.thread = threading.Thread(target=run, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.source = "nvidia-smi"
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.device_index),
+                     "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                     "clocks_event_reasons.hw_thermal_slowdown,"
+                     "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                     "--format=csv,noheader,nounits", "-lms", "100"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                self.proc = None
         return self
 
     def __exit__(self, *exc):
-        self.out = ""
+        self.stop = True
+        if self.thread is not None:
+            self.thread.join(timeout=2)
         if self.proc is not None:
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                out, _ = self.proc.communicate(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                self.out, _ = self.proc.communicate()
+                out, _ = self.proc.communicate()
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for line in (out or "").strip().splitlines():
+                parts = [p.strip() for p in line.split(",")]
+                try:
+                    self.samples.append(float(parts[0]))
+                    self.max_mhz = float(parts[1])
+                except (ValueError, IndexError):
+                    continue
+                for n, v in zip(names, parts[2:6]):
+                    if v.lower().startswith("active"):
+                        self.reasons.add(n)
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in (self.out or "").strip().splitlines():
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"],
+                    "samples": 0, "source": self.source}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples),
+                "source": self.source}
 
 
 def dist_setup():

@@ -14,10 +14,11 @@
 //              warp 0      TMA producer (K_j, V_j once; Q_i, dO_i, L2_i, Ds_i
 //                          per step into a ring)
 //              warp 1      MMA issuer + TMEM owner
-//              warps 4..7  "compute": thread = key row; P^T = exp2(S^T c - L2)
+//              warps 4..11 "compute", two warpgroups splitting the 128 query
+//                          columns: thread = key row; P^T = exp2(S^T c - L2)
 //                          to TMEM (bf16), dS^T = P^T o (scale dP^T - Ds) to
 //                          smem (bf16, 128-B swizzle)
-//              warps 8..11 "dQ": thread = query row; dQ_i partial TMEM ->
+//              warps 12..15 "dQ": thread = query row; dQ_i partial TMEM ->
 //                          smem -> TMA reduce-add (fp32) into the accumulator
 //            MMAs per step: S^T = K Q^T, dP^T = V dO^T (both SS, K-major),
 //            dV += P^T dO (TS), dK += dS^T Q (SS, B MN-major),
@@ -34,7 +35,11 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------- preprocess
-// TPR threads per row, each owning 16 bytes of O and dO.
+// TPR threads per row, each owning 16 bytes of O and dO; every thread handles
+// kPreRows rows (all loads issued before any use, for memory-level
+// parallelism).
+constexpr int kPreRows = 4;
+
 template <typename T, int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const T* __restrict__ O,
                                                       const T* __restrict__ dO,
@@ -45,56 +50,86 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const T* __restrict__ O,
                                                       float scale) {
   constexpr int EPV = 16 / sizeof(T);  // elements per 16-B vector
   constexpr int TPR = D / EPV;         // threads per row
-  constexpr int RPB = 256 / TPR;       // rows per block-iteration
+  constexpr int RPB = 256 / TPR;       // rows per block per pass
   const int sub = threadIdx.x % TPR;
-  for (long long row = static_cast<long long>(blockIdx.x) * RPB + threadIdx.x / TPR; row < rows;
-       row += static_cast<long long>(gridDim.x) * RPB) {
-    const size_t base = static_cast<size_t>(row) * D + sub * EPV;
-    const uint4 ov = __ldg(reinterpret_cast<const uint4*>(O + base));
-    const uint4 gv = __ldg(reinterpret_cast<const uint4*>(dO + base));
+  const long long row0 = static_cast<long long>(blockIdx.x) * RPB * kPreRows + threadIdx.x / TPR;
+  uint4 ov[kPreRows], gv[kPreRows];
+#pragma unroll
+  for (int u = 0; u < kPreRows; ++u) {
+    const long long row = row0 + static_cast<long long>(u) * RPB;
+    if (row < rows) {
+      const size_t base = static_cast<size_t>(row) * D + sub * EPV;
+      ov[u] = __ldg(reinterpret_cast<const uint4*>(O + base));
+      gv[u] = __ldg(reinterpret_cast<const uint4*>(dO + base));
+    } else {
+      ov[u] = gv[u] = make_uint4(0, 0, 0, 0);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kPreRows; ++u) {
+    const long long row = row0 + static_cast<long long>(u) * RPB;
     float acc = 0.f;
     if constexpr (sizeof(T) == 2) {
-      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
-      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov[u]);
+      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv[u]);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float2 a = __bfloat1622float2(o2[k]), b = __bfloat1622float2(g2[k]);
-        acc = fmaf(a.x, b.x, acc);
-        acc = fmaf(a.y, b.y, acc);
+        const float2 x = __bfloat1622float2(o2[k]), y = __bfloat1622float2(g2[k]);
+        acc = fmaf(x.x, y.x, acc);
+        acc = fmaf(x.y, y.y, acc);
       }
     } else {
-      const float* o4 = reinterpret_cast<const float*>(&ov);
-      const float* g4 = reinterpret_cast<const float*>(&gv);
+      const float* o4 = reinterpret_cast<const float*>(&ov[u]);
+      const float* g4 = reinterpret_cast<const float*>(&gv[u]);
 #pragma unroll
       for (int k = 0; k < 4; ++k) acc = fmaf(o4[k], g4[k], acc);
     }
+    // rows are whole warps' worth (rows % 128 == 0), so the shuffle is safe
 #pragma unroll
     for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (sub == 0) {
-      ds_row[row] = acc * scale;
-      l2_row[row] = lse[row] * kLog2e;
-    }
-    // zero this thread's share of the fp32 accumulator row (D floats)
-    float4* z = reinterpret_cast<float4*>(dq_acc + static_cast<size_t>(row) * D);
+    if (row < rows) {
+      if (sub == 0) {
+        ds_row[row] = acc * scale;
+        l2_row[row] = lse[row] * kLog2e;
+      }
+      // zero this thread's share of the fp32 accumulator row (D floats)
+      if (dq_acc != nullptr) {
+        float4* z = reinterpret_cast<float4*>(dq_acc + static_cast<size_t>(row) * D);
 #pragma unroll
-    for (int k = sub; k < D / 4; k += TPR) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = sub; k < D / 4; k += TPR) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
   }
 }
 
 // ---------------------------------------------------------------- dQ cast
+// Each thread converts kPostVecs groups of 8 fp32 -> 8 bf16.
+constexpr int kPostVecs = 4;
+
 __global__ void __launch_bounds__(256) bwd_post_kernel(const float* __restrict__ acc,
                                                        __nv_bfloat16* __restrict__ dq,
                                                        long long n8) {
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const float4 a = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i);
-    const float4 b = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i + 1);
-    uint4 v;
-    v.x = pack_bf16(a.x, a.y);
-    v.y = pack_bf16(a.z, a.w);
-    v.z = pack_bf16(b.x, b.y);
-    v.w = pack_bf16(b.z, b.w);
-    reinterpret_cast<uint4*>(dq)[i] = v;
+  const long long i0 = static_cast<long long>(blockIdx.x) * 256 * kPostVecs + threadIdx.x;
+  float4 a[kPostVecs], b[kPostVecs];
+#pragma unroll
+  for (int u = 0; u < kPostVecs; ++u) {
+    const long long i = i0 + static_cast<long long>(u) * 256;
+    if (i < n8) {
+      a[u] = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i);
+      b[u] = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i + 1);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kPostVecs; ++u) {
+    const long long i = i0 + static_cast<long long>(u) * 256;
+    if (i < n8) {
+      uint4 v;
+      v.x = pack_bf16(a[u].x, a[u].y);
+      v.y = pack_bf16(a[u].z, a[u].w);
+      v.z = pack_bf16(b[u].x, b[u].y);
+      v.w = pack_bf16(b[u].z, b[u].w);
+      reinterpret_cast<uint4*>(dq)[i] = v;
+    }
   }
 }
 
@@ -122,7 +157,9 @@ struct BwdCfg {
   static constexpr int OFF_L2 = OFF_DQ + 2 * BLK_BYTES;
   static constexpr int OFF_DSR = OFF_L2 + QST * 512;
   static constexpr int SMEM_BYTES = 1024 + OFF_DSR + QST * 512;
-  static constexpr int THREADS = 384;
+  static constexpr int THREADS = 512;
+  // S_{n+1} may be issued before dK_n only when the ring holds two steps.
+  static constexpr bool EARLY_S = QST >= 2;
 };
 
 enum : int {
@@ -172,8 +209,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
     mbar_init(bar(C_KVFULL), 1);
     mbar_init(bar(C_SFULL), 1);
     mbar_init(bar(C_DPFULL), 1);
-    mbar_init(bar(C_PFULL), 128);
-    mbar_init(bar(C_DSFULL), 128);
+    mbar_init(bar(C_PFULL), 256);
+    mbar_init(bar(C_DSFULL), 256);
     mbar_init(bar(C_DSEMPTY), 1);
     mbar_init(bar(C_DQFULL), 1);
     mbar_init(bar(C_DQFREE), 128);
@@ -182,7 +219,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
     for (int s = 0; s < QST; ++s) {
       mbar_init(qfull(s), 1);
       mbar_init(dofull(s), 1);
-      mbar_init(qempty(s), 1 + 4);  // MMA commit + one arrive per compute warp
+      mbar_init(qempty(s), 1 + 8);  // MMA commit + one arrive per compute warp
     }
     fence_barrier_init();
   }
@@ -252,13 +289,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
       constexpr uint32_t idDV = make_idesc<MmaKind::kBF16>(128, D, false, true);
       constexpr uint32_t idDK = make_idesc<MmaKind::kBF16>(128, D, false, true);
       constexpr uint32_t idDQ = make_idesc<MmaKind::kBF16>(128, D, true, true);
-      bool ok = mbar_wait(bar(C_KVFULL), 0, abort, 22, status);
-      for (int n = 0; ok && n < nsteps; ++n) {
+      auto issue_s = [&](int n) {  // S^T = K_j Q_i^T
         const int s = n % QST;
-        const uint32_t ph = (n / QST) & 1;
-        // S^T = K_j Q_i^T
-        if (!mbar_wait(qfull(s), ph, abort, 23, status)) break;
-        tc_fence_after();
 #pragma unroll
         for (int k = 0; k < C::NK_QK; ++k) {
           const uint32_t off = (k / 4) * C::BLK_BYTES + (k % 4) * 32;
@@ -266,11 +298,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
                                  sdesc_sw128(sQ(s) + off, 16, 1024), idS, k > 0 ? 1u : 0u);
         }
         mma_commit(bar(C_SFULL));
-        // dP^T = V_j dO_i^T
-        if (!mbar_wait(dofull(s), ph, abort, 24, status)) break;
-        if (C::DQ_ALIAS_DP && n > 0 && !mbar_wait(bar(C_DQFREE), (n - 1) & 1, abort, 25, status))
-          break;
-        tc_fence_after();
+      };
+      auto issue_dp = [&](int n) {  // dP^T = V_j dO_i^T
+        const int s = n % QST;
 #pragma unroll
         for (int k = 0; k < C::NK_QK; ++k) {
           const uint32_t off = (k / 4) * C::BLK_BYTES + (k % 4) * 32;
@@ -278,6 +308,30 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
                                  sdesc_sw128(sDO(s) + off, 16, 1024), idS, k > 0 ? 1u : 0u);
         }
         mma_commit(bar(C_DPFULL));
+      };
+      auto wait_q = [&](int n, uint32_t id) {
+        return mbar_wait(qfull(n % QST), (n / QST) & 1, abort, id, status);
+      };
+      auto wait_do = [&](int n, uint32_t id) {
+        return mbar_wait(dofull(n % QST), (n / QST) & 1, abort, id, status);
+      };
+      // Issue order per step n (ring depth 2): dV_n, S_{n+1}, dK_n, dQ_n, dP_{n+1}
+      // so the next step's S and dP run while the compute warps finish step n.
+      // With a ring of depth 1, Q_{n+1} only lands after dK_n, so S_{n+1}
+      // moves behind dK_n.
+      bool ok = mbar_wait(bar(C_KVFULL), 0, abort, 22, status) && wait_q(0, 23);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        ok = wait_do(0, 24);
+        if (ok) {
+          tc_fence_after();
+          issue_dp(0);
+        }
+      }
+      for (int n = 0; ok && n < nsteps; ++n) {
+        const int s = n % QST;
+        const bool more = n + 1 < nsteps;
         // dV += P^T dO_i
         if (!mbar_wait(bar(C_PFULL), n & 1, abort, 26, status)) break;
         tc_fence_after();
@@ -286,7 +340,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
           mma_ts<MmaKind::kBF16>(tmem + C::DV_COL, tmem + C::P_COL + k * 8,
                                  sdesc_sw128(sDO(s) + k * 16 * 128, C::BLK_BYTES, 1024), idDV,
                                  (n > 0 || k > 0) ? 1u : 0u);
-        // dK += dS^T Q_i ; dQ_i = dS K_j
+        if (C::EARLY_S && more) {
+          if (!wait_q(n + 1, 23)) break;
+          tc_fence_after();
+          issue_s(n + 1);
+        }
+        // dK += dS^T Q_i
         if (!mbar_wait(bar(C_DSFULL), n & 1, abort, 27, status)) break;
         tc_fence_after();
 #pragma unroll
@@ -297,6 +356,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
                                  (n > 0 || k > 0) ? 1u : 0u);
         }
         mma_commit(qempty(s));
+        if (!C::EARLY_S && more) {
+          if (!wait_q(n + 1, 23)) break;
+          tc_fence_after();
+          issue_s(n + 1);
+        }
+        // dQ_i = dS K_j
         if (!C::DQ_ALIAS_DP && n > 0 && !mbar_wait(bar(C_DQFREE), (n - 1) & 1, abort, 28, status))
           break;
         tc_fence_after();
@@ -308,15 +373,26 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
                                  k > 0 ? 1u : 0u);
         mma_commit(bar(C_DSEMPTY));
         mma_commit(bar(C_DQFULL));
+        if (more) {
+          if (!wait_do(n + 1, 24)) break;
+          // d=128: dP shares its columns with dQ_n, which must be drained first
+          if (C::DQ_ALIAS_DP && !mbar_wait(bar(C_DQFREE), n & 1, abort, 25, status)) break;
+          tc_fence_after();
+          issue_dp(n + 1);
+        }
       }
       mma_commit(bar(C_FINAL));
       mma_commit(bar(C_DRAIN));
       mbar_wait_drain(bar(C_DRAIN), 0, 29, status);
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ compute
+    // Two warpgroups: half 0 owns query columns 0..63 of every step, half 1
+    // columns 64..127.  Thread = key row kr (TMEM lane).
+    const int half = (warp - 4) >> 2;
     const int quad = warp & 3;
-    const int kr = quad * 32 + lane;  // key row within tile j == TMEM lane
+    const int kr = quad * 32 + lane;
+    const int q0 = 64 * half;
     const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const float c = a.scale * kLog2e;
     bool ok = true;
@@ -331,18 +407,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
         break;
       }
       tc_fence_after();
-      uint32_t u0[32], u1[32], u2[32], u3[32];
-      tmem_ld32(trow + C::S_COL + 0, u0);
-      tmem_ld32(trow + C::S_COL + 32, u1);
-      tmem_ld32(trow + C::S_COL + 64, u2);
-      tmem_ld32(trow + C::S_COL + 96, u3);
+      uint32_t u0[32], u1[32];
+      tmem_ld32(trow + C::S_COL + q0, u0);
+      tmem_ld32(trow + C::S_COL + q0 + 32, u1);
       tmem_ld_wait(u0);
       reg_fence(u1);
-      reg_fence(u2);
-      reg_fence(u3);
-      const float* l2 = l2_s + s * 128;
+      const float* l2 = l2_s + s * 128 + q0;
       const bool diag = a.causal && i == j;
-      uint32_t pk[64];  // P^T row, bf16 pairs (query 2t in the low half)
+      uint32_t pk[32];  // P^T row, bf16 pairs (query 2t in the low half)
       auto make_p = [&](const uint32_t (&u)[32], int c0) {
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
@@ -350,25 +422,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
           float p0 = ex2(fmaf(__uint_as_float(u[2 * t]), c, -lv.x));
           float p1 = ex2(fmaf(__uint_as_float(u[2 * t + 1]), c, -lv.y));
           if (diag) {
-            if (c0 + 2 * t < kr) p0 = 0.f;
-            if (c0 + 2 * t + 1 < kr) p1 = 0.f;
+            if (q0 + c0 + 2 * t < kr) p0 = 0.f;
+            if (q0 + c0 + 2 * t + 1 < kr) p1 = 0.f;
           }
           pk[c0 / 2 + t] = pack_bf16(p0, p1);
         }
       };
       make_p(u0, 0);
       make_p(u1, 32);
-      make_p(u2, 64);
-      make_p(u3, 96);
-      {
-        uint32_t w[32];
-#pragma unroll
-        for (int t = 0; t < 32; ++t) w[t] = pk[t];
-        tmem_st32(trow + C::P_COL, w);
-#pragma unroll
-        for (int t = 0; t < 32; ++t) w[t] = pk[32 + t];
-        tmem_st32(trow + C::P_COL + 32, w);
-      }
+      tmem_st32(trow + C::P_COL + q0 / 2, pk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(C_PFULL));
@@ -380,17 +442,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
         break;
       }
       tc_fence_after();
-      const float* dsr = dsr_s + s * 128;
-      uint8_t* dsrow = smem + C::OFF_DS + kr * 128;
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t v[32];
-        tmem_ld32(trow + C::DP_COL + 32 * cc, v);
-        tmem_ld_wait(v);
+      uint32_t v0[32], v1[32];
+      tmem_ld32(trow + C::DP_COL + q0, v0);
+      tmem_ld32(trow + C::DP_COL + q0 + 32, v1);
+      tmem_ld_wait(v0);
+      reg_fence(v1);
+      const float* dsr = dsr_s + s * 128 + q0;
+      uint8_t* dsrow = smem + C::OFF_DS + half * C::BLK_BYTES + kr * 128;
+      auto make_ds = [&](const uint32_t (&v)[32], int c0) {
         uint32_t o[16];
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
-          const int q = 32 * cc + 2 * t;
+          const int q = c0 + 2 * t;
           const uint32_t pp = pk[q / 2];
           const float p0 = __uint_as_float(pp << 16), p1 = __uint_as_float(pp & 0xffff0000u);
           const float2 dv = *reinterpret_cast<const float2*>(dsr + q);
@@ -398,74 +461,67 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
           const float d1 = p1 * fmaf(__uint_as_float(v[2 * t + 1]), a.scale, -dv.y);
           o[t] = pack_bf16(d0, d1);
         }
-        // 32 queries -> 64 B of row kr: block (32cc)/64, chunks 4*(cc%2) .. +3
-        const int blk = cc / 2;
+        // 32 queries = 64 B = chunks c0/8 .. c0/8 + 3 of this 128-B row
 #pragma unroll
         for (int t4 = 0; t4 < 4; ++t4) {
-          const int chunk = 4 * (cc % 2) + t4;
-          *reinterpret_cast<uint4*>(dsrow + blk * C::BLK_BYTES + ((chunk ^ (kr & 7)) << 4)) =
+          const int chunk = c0 / 8 + t4;
+          *reinterpret_cast<uint4*>(dsrow + ((chunk ^ (kr & 7)) << 4)) =
               make_uint4(o[4 * t4], o[4 * t4 + 1], o[4 * t4 + 2], o[4 * t4 + 3]);
         }
-      }
+      };
+      make_ds(v0, 0);
+      make_ds(v1, 32);
       fence_proxy_async();
       tc_fence_before();
       mbar_arrive(bar(C_DSFULL));
       __syncwarp();
       if (lane == 0) mbar_arrive(qempty(s));
     }
-    // epilogue: dV, dK rows of this key tile
+    // epilogue: half 0 writes dV rows, half 1 writes dK rows of this key tile
     if (ok) ok = mbar_wait_warp(bar(C_FINAL), 0, abort, 35, status);
     if (ok) {
       tc_fence_after();
-      const size_t row = (static_cast<size_t>(b) * a.Hkv + g) * a.N + static_cast<size_t>(j) * kTile + kr;
-      __nv_bfloat16* dv_out = static_cast<__nv_bfloat16*>(a.dV) + row * D;
-      __nv_bfloat16* dk_out = static_cast<__nv_bfloat16*>(a.dK) + row * D;
+      const size_t row =
+          (static_cast<size_t>(b) * a.Hkv + g) * a.N + static_cast<size_t>(j) * kTile + kr;
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(half == 0 ? a.dV : a.dK) + row * D;
+      const uint32_t col = half == 0 ? C::DV_COL : C::DK_COL;
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        __nv_bfloat16* dst = which == 0 ? dv_out : dk_out;
-        const uint32_t col = which == 0 ? C::DV_COL : C::DK_COL;
+      for (int cc = 0; cc < D; cc += 32) {
+        uint32_t v[32];
+        tmem_ld32(trow + col + cc, v);
+        tmem_ld_wait(v);
 #pragma unroll
-        for (int cc = 0; cc < D; cc += 32) {
-          uint32_t v[32];
-          tmem_ld32(trow + col + cc, v);
-          tmem_ld_wait(v);
-#pragma unroll
-          for (int t4 = 0; t4 < 4; ++t4) {
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(v[8 * t4 + 0]), __uint_as_float(v[8 * t4 + 1]));
-            w.y = pack_bf16(__uint_as_float(v[8 * t4 + 2]), __uint_as_float(v[8 * t4 + 3]));
-            w.z = pack_bf16(__uint_as_float(v[8 * t4 + 4]), __uint_as_float(v[8 * t4 + 5]));
-            w.w = pack_bf16(__uint_as_float(v[8 * t4 + 6]), __uint_as_float(v[8 * t4 + 7]));
-            *reinterpret_cast<uint4*>(dst + cc + 8 * t4) = w;
-          }
+        for (int t4 = 0; t4 < 4; ++t4) {
+          uint4 w;
+          w.x = pack_bf16(__uint_as_float(v[8 * t4 + 0]), __uint_as_float(v[8 * t4 + 1]));
+          w.y = pack_bf16(__uint_as_float(v[8 * t4 + 2]), __uint_as_float(v[8 * t4 + 3]));
+          w.z = pack_bf16(__uint_as_float(v[8 * t4 + 4]), __uint_as_float(v[8 * t4 + 5]));
+          w.w = pack_bf16(__uint_as_float(v[8 * t4 + 6]), __uint_as_float(v[8 * t4 + 7]));
+          *reinterpret_cast<uint4*>(dst + cc + 8 * t4) = w;
         }
       }
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 12) {
     // ------------------------------------------------------------ dQ
     const int quad = warp & 3;
     const int qr = quad * 32 + lane;  // query row == TMEM lane of the dQ tile
     const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    const bool leader = warp == 8 && lane == 0;
-    bool ok = true;
+    const bool leader = warp == 12 && lane == 0;
     for (int n = 0; n < nsteps; ++n) {
       int h, i;
       step_hi(n, h, i);
       const int bh = b * a.H + h;
       // the whole warpgroup unwinds together: it meets at named barriers below
-      if (!named_bar_and(2, 128, mbar_wait_warp(bar(C_DQFULL), n & 1, abort, 36, status))) {
-        ok = false;
-        break;
-      }
+      if (!named_bar_and(2, 128, mbar_wait_warp(bar(C_DQFULL), n & 1, abort, 36, status))) break;
       tc_fence_after();
 #pragma unroll
-      for (int half = 0; half < D / 64; ++half) {
+      for (int hh = 0; hh < D / 64; ++hh) {
         uint32_t v0[32], v1[32];
-        tmem_ld32(trow + C::DQ_COL + 64 * half, v0);
-        tmem_ld32(trow + C::DQ_COL + 64 * half + 32, v1);
+        tmem_ld32(trow + C::DQ_COL + 64 * hh, v0);
+        tmem_ld32(trow + C::DQ_COL + 64 * hh + 32, v1);
         tmem_ld_wait(v0);
         reg_fence(v1);
-        if (half == D / 64 - 1) {
+        if (hh == D / 64 - 1) {
           tc_fence_before();
           mbar_arrive(bar(C_DQFREE));
         }
@@ -485,13 +541,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
         named_bar_sync(2, 128);
         if (leader) {
           for (int box = 0; box < 2; ++box)
-            tma_reduce_add_3d(&a.tmdQacc, sDQ + box * C::BLK_BYTES, 64 * half + 32 * box,
+            tma_reduce_add_3d(&a.tmdQacc, sDQ + box * C::BLK_BYTES, 64 * hh + 32 * box,
                               i * kTile, bh);
           bulk_commit();
         }
       }
     }
-    (void)ok;
     if (leader) bulk_wait0();
   }
   tc_fence_before();
@@ -503,13 +558,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
   }
 }
 
-unsigned grid_for(long long work_items, int per_block) {
-  long long blocks = (work_items + per_block - 1) / per_block;
-  const long long cap = 152LL * 16;
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
-  return static_cast<unsigned>(blocks);
-}
 
 template <int D>
 cudaError_t launch_main_t(const BwdArgs& a, cudaStream_t stream) {
@@ -527,26 +575,24 @@ cudaError_t launch_main_t(const BwdArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t stream) {
   const long long rows = static_cast<long long>(a.B) * a.H * a.N;
-  if (a.dtype == 0) {
-    const int tpr = a.d / 8;
-    const unsigned grid = grid_for(rows, 256 / tpr);
-    if (a.d == 64)
-      bwd_pre_kernel<__nv_bfloat16, 64><<<grid, 256, 0, stream>>>(
-          static_cast<const __nv_bfloat16*>(a.O), static_cast<const __nv_bfloat16*>(a.dO), a.lse,
-          a.delta, a.lse2, a.dq_acc, rows, a.scale);
-    else
-      bwd_pre_kernel<__nv_bfloat16, 128><<<grid, 256, 0, stream>>>(
-          static_cast<const __nv_bfloat16*>(a.O), static_cast<const __nv_bfloat16*>(a.dO), a.lse,
-          a.delta, a.lse2, a.dq_acc, rows, a.scale);
-  } else {
-    const unsigned grid = grid_for(rows, 256 / (a.d / 4));
-    if (a.d == 64)
-      bwd_pre_kernel<float, 64><<<grid, 256, 0, stream>>>(
-          static_cast<const float*>(a.O), static_cast<const float*>(a.dO), a.lse, a.delta, a.lse2,
-          a.dq_acc, rows, a.scale);
-    else
-      return cudaErrorInvalidValue;
-  }
+  const int esize = a.dtype == 0 ? 2 : 4;
+  const int tpr = a.d * esize / 16;
+  const long long per_block = static_cast<long long>(256 / tpr) * kPreRows;
+  const unsigned grid = static_cast<unsigned>((rows + per_block - 1) / per_block);
+  if (a.dtype == 0 && a.d == 64)
+    bwd_pre_kernel<__nv_bfloat16, 64><<<grid, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(a.O), static_cast<const __nv_bfloat16*>(a.dO), a.lse,
+        a.delta, a.lse2, a.dq_acc, rows, a.scale);
+  else if (a.dtype == 0 && a.d == 128)
+    bwd_pre_kernel<__nv_bfloat16, 128><<<grid, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(a.O), static_cast<const __nv_bfloat16*>(a.dO), a.lse,
+        a.delta, a.lse2, a.dq_acc, rows, a.scale);
+  else if (a.dtype == 1 && a.d == 64)
+    bwd_pre_kernel<float, 64><<<grid, 256, 0, stream>>>(
+        static_cast<const float*>(a.O), static_cast<const float*>(a.dO), a.lse, a.delta, a.lse2,
+        a.dq_acc, rows, a.scale);
+  else
+    return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 
@@ -558,7 +604,8 @@ cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_bwd_post(const BwdArgs& a, cudaStream_t stream) {
   const long long n8 = static_cast<long long>(a.B) * a.H * a.N * a.d / 8;
-  bwd_post_kernel<<<grid_for(n8, 256), 256, 0, stream>>>(
+  const long long per_block = 256LL * kPostVecs;
+  bwd_post_kernel<<<static_cast<unsigned>((n8 + per_block - 1) / per_block), 256, 0, stream>>>(
       a.dq_acc, static_cast<__nv_bfloat16*>(a.dQ), n8);
   return cudaGetLastError();
 }

@@ -52,7 +52,7 @@ struct FwdCfg {
 };
 
 // mbarrier slots
-enum : int { B_QFULL = 0, B_SFULL, B_SFREE, B_PFULL, B_ODONE, B_DRAIN, B_KFULL };
+enum : int { B_QFULL = 0, B_SFULL, B_SFREE, B_PFULL, B_ODONE, B_DRAIN, B_QREADY, B_KFULL };
 // K_FULL[s] = B_KFULL + s, V_FULL[s] = B_KFULL + ST + s, KV_EMPTY[s] = B_KFULL + 2 ST + s
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -68,7 +68,8 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  __shared__ __align__(8) uint64_t bars[B_KFULL + 4 * ST];  // + VT_FULL[s] = B_KFULL + 3 ST + s
+  // + VT_FULL[s] = B_KFULL + 3 ST + s, KREADY[s] = B_KFULL + 4 ST + s (tf32)
+  __shared__ __align__(8) uint64_t bars[B_KFULL + 5 * ST];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -98,7 +99,8 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
     mbar_init(bar(B_ODONE), 1);
     mbar_init(bar(B_DRAIN), 1);
     for (int s = 0; s < 3 * ST; ++s) mbar_init(bar(B_KFULL + s), 1);
-    for (int s = 0; s < ST; ++s) mbar_init(bar(B_KFULL + 3 * ST + s), 128);
+    for (int s = 0; s < 2 * ST; ++s) mbar_init(bar(B_KFULL + 3 * ST + s), 128);
+    mbar_init(bar(B_QREADY), 128);
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -156,7 +158,8 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
       constexpr uint32_t idPV = make_idesc<KIND>(128, D, false, !C::TRANSPOSE_V);
       auto issue_s = [&](int j) -> bool {
         const int s = j % ST;
-        if (!mbar_wait(bar(B_KFULL + s), (j / ST) & 1, abort, 3, status)) return false;
+        const int kbar = C::TRANSPOSE_V ? B_KFULL + 4 * ST + s : B_KFULL + s;
+        if (!mbar_wait(bar(kbar), (j / ST) & 1, abort, 3, status)) return false;
         tc_fence_after();
         const uint32_t sK = sKV + (2 * s) * C::TILE_BYTES;
 #pragma unroll
@@ -168,7 +171,8 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
         mma_commit(bar(B_SFULL));
         return true;
       };
-      bool ok = mbar_wait(bar(B_QFULL), 0, abort, 4, status) && issue_s(0);
+      bool ok = mbar_wait(bar(C::TRANSPOSE_V ? B_QREADY : B_QFULL), 0, abort, 4, status) &&
+                issue_s(0);
       for (int j = 0; ok && j < nkv; ++j) {
         if (j + 1 < nkv) {
           // S_{j+1} overwrites S once the softmax has read S_j.
@@ -199,32 +203,59 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
       mbar_wait_drain(bar(B_DRAIN), 0, 8, status);
     }
   } else if (warp >= 6) {
-    // ------------------------------------------------------------ V transposer
-    // (tf32 only) thread t = key row t of V_j; writes column t of V^T.
+    // ------------------------------------------------------------ tf32 prep
+    // (tf32 only) rounds Q (once) and each K tile to tf32 in place, and
+    // writes V_j transposed (and rounded) as V^T [d][keys]: thread t = key
+    // row t of V_j writes column t of V^T.
     if constexpr (C::TRANSPOSE_V) {
       const int t = threadIdx.x - 192;
-      for (int j = 0; j < nkv; ++j) {
-        const int s = j % ST;
-        if (!mbar_wait_warp(bar(B_KFULL + ST + s), (j / ST) & 1, abort, 12, status)) break;
-        const uint8_t* vrow = smem + (sKV - sQ) + (2 * s + 1) * C::TILE_BYTES + t * 128;
-        uint8_t* vt = smem + (sVT - sQ) + s * C::VT_BYTES + (t / 32) * C::VT_BLK_BYTES + (t % 4) * 4;
-        const int tchunk = (t % 32) / 4;
+      // Elementwise rounding of a whole tile: thread t owns bytes
+      // [t*TILE/128, (t+1)*TILE/128); the layout does not matter.
+      auto round_tile = [&](uint32_t tile) {
+        uint4* p = reinterpret_cast<uint4*>(smem + (tile - sQ) + t * (C::TILE_BYTES / 128));
 #pragma unroll
-        for (int blk = 0; blk < C::NBLK; ++blk) {
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            const float4 x =
-                *reinterpret_cast<const float4*>(vrow + blk * C::BLK_BYTES + ((ch ^ (t & 7)) << 4));
-            const float xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c = blk * 32 + ch * 4 + e;  // column of V = row of V^T
-              *reinterpret_cast<float*>(vt + c * 128 + ((tchunk ^ (c & 7)) << 4)) = xs[e];
-            }
-          }
+        for (int k = 0; k < C::TILE_BYTES / 128 / 16; ++k) {
+          uint4 x = p[k];
+          x.x = tf32_rna(__uint_as_float(x.x));
+          x.y = tf32_rna(__uint_as_float(x.y));
+          x.z = tf32_rna(__uint_as_float(x.z));
+          x.w = tf32_rna(__uint_as_float(x.w));
+          p[k] = x;
         }
         fence_proxy_async();
-        mbar_arrive(bar(B_KFULL + 3 * ST + s));
+      };
+      if (mbar_wait_warp(bar(B_QFULL), 0, abort, 13, status)) {
+        round_tile(sQ);
+        mbar_arrive(bar(B_QREADY));
+        for (int j = 0; j < nkv; ++j) {
+          const int s = j % ST;
+          const uint32_t ph = (j / ST) & 1;
+          if (!mbar_wait_warp(bar(B_KFULL + s), ph, abort, 14, status)) break;
+          round_tile(sKV + (2 * s) * C::TILE_BYTES);
+          mbar_arrive(bar(B_KFULL + 4 * ST + s));
+          if (!mbar_wait_warp(bar(B_KFULL + ST + s), ph, abort, 12, status)) break;
+          const uint8_t* vrow = smem + (sKV - sQ) + (2 * s + 1) * C::TILE_BYTES + t * 128;
+          uint8_t* vt =
+              smem + (sVT - sQ) + s * C::VT_BYTES + (t / 32) * C::VT_BLK_BYTES + (t % 4) * 4;
+          const int tchunk = (t % 32) / 4;
+#pragma unroll
+          for (int blk = 0; blk < C::NBLK; ++blk) {
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+              const float4 x = *reinterpret_cast<const float4*>(vrow + blk * C::BLK_BYTES +
+                                                               ((ch ^ (t & 7)) << 4));
+              const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int c = blk * 32 + ch * 4 + e;  // column of V = row of V^T
+                *reinterpret_cast<uint32_t*>(vt + c * 128 + ((tchunk ^ (c & 7)) << 4)) =
+                    tf32_rna(xs[e]);
+              }
+            }
+          }
+          fence_proxy_async();
+          mbar_arrive(bar(B_KFULL + 3 * ST + s));
+        }
       }
     }
   } else {
@@ -265,9 +296,17 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
         for (int i = 0; i < 128; ++i)
           if (i > r) sv[i] = -INFINITY;
       }
-      float mx = sv[0];
+      // row max as a tree (8 independent chains), not a 128-long chain
+      float mv[8];
 #pragma unroll
-      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, sv[i]);
+      for (int k = 0; k < 8; ++k) mv[k] = sv[k];
+#pragma unroll
+      for (int i = 8; i < 128; i += 8) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mv[k] = fmaxf(mv[k], sv[i + k]);
+      }
+      const float mx = fmaxf(fmaxf(fmaxf(mv[0], mv[1]), fmaxf(mv[2], mv[3])),
+                             fmaxf(fmaxf(mv[4], mv[5]), fmaxf(mv[6], mv[7])));
       // PV_{j-1} must be complete before P is overwritten or O rescaled.
       if (j > 0) {
         if (!mbar_wait_warp(bar(B_ODONE), (j - 1) & 1, abort, 10, status)) {
@@ -284,14 +323,19 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
         m_ref = m_new;
       }
       const float moff = -m_ref * c;
-      float rs = 0.f;
+      // exponent arguments with packed fp32x2 FMAs; row sum in 4 packed chains
+      const float2 c2 = make_float2(c, c), moff2 = make_float2(moff, moff);
+      float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                       make_float2(0.f, 0.f)};
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         float p[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          p[i] = ex2(fmaf(sv[32 * cc + i], c, moff));
-          rs += p[i];
+        for (int i = 0; i < 32; i += 2) {
+          const float2 x = __ffma2_rn(make_float2(sv[32 * cc + i], sv[32 * cc + i + 1]), c2, moff2);
+          p[i] = ex2(x.x);
+          p[i + 1] = ex2(x.y);
+          rs2[(i >> 1) & 3] = __fadd2_rn(rs2[(i >> 1) & 3], make_float2(p[i], p[i + 1]));
         }
         if constexpr (KIND == MmaKind::kBF16) {
           uint32_t pk[16];
@@ -305,6 +349,8 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
           tmem_st32(trow + C::P_COL + 32 * cc, pk);
         }
       }
+      const float2 r01 = __fadd2_rn(rs2[0], rs2[1]), r23 = __fadd2_rn(rs2[2], rs2[3]);
+      const float rs = (r01.x + r01.y) + (r23.x + r23.y);
       l = l * alpha + rs;
       // O rescale after P: the S registers are dead by now
       if (j > 0 && __any_sync(0xffffffffu, need)) {

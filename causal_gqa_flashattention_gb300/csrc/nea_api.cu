@@ -74,6 +74,22 @@ bool encode_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esi
          CUDA_SUCCESS;
 }
 
+// 3-D view {N, d, heads} of a transposed fp32 [heads][d][N] array: boxes of
+// 32 columns (128 B) x d rows, 128-byte swizzle (K-major tf32 operands).
+bool encode_3d_t(CUtensorMap* m, const void* base, int d, int N, long long heads) {
+  EncodeTiledFn enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(d),
+                        static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(N) * 4,
+                           static_cast<cuuint64_t>(N) * 4 * static_cast<cuuint64_t>(d)};
+  cuuint32_t box[3] = {32, static_cast<cuuint32_t>(d), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Shape / option checks shared by every entry point.  `bwd`: the checks of
@@ -90,22 +106,35 @@ int check_common(int B, int H, int Hkv, int N, int d, float scale, int causal, i
   if (bh > (1LL << 24) || N > (1 << 24)) return NEA_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return NEA_ERR_UNSUPPORTED;
   if (N % kTile != 0) return NEA_ERR_UNSUPPORTED;
-  if (dtype == NEA_F32 && (bwd || d != 64)) return NEA_ERR_UNSUPPORTED;
+  (void)bwd;
+  if (dtype == NEA_F32 && d != 64) return NEA_ERR_UNSUPPORTED;
   return NEA_OK;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// bf16: D, L2, fp32 dQ accumulator.  fp32: D, L2, Q^T, dO^T, K^T (tf32).
 struct WsLayout {
-  size_t delta, lse2, dqacc, total;
+  size_t delta, lse2, dqacc, qt, dot, kt, total;
 };
-WsLayout ws_layout(int B, int H, int N, int d, int dtype) {
+WsLayout ws_layout(int B, int H, int Hkv, int N, int d, int dtype) {
   const size_t rows = static_cast<size_t>(B) * H * N;
+  const size_t kvrows = static_cast<size_t>(B) * Hkv * N;
   WsLayout w;
   w.delta = 0;
   w.lse2 = align256(rows * sizeof(float));
-  w.dqacc = w.lse2 + align256(rows * sizeof(float));
-  w.total = w.dqacc + (dtype == NEA_BF16 ? align256(rows * d * sizeof(float)) : 0);
+  w.dqacc = w.qt = w.dot = w.kt = 0;
+  size_t end = w.lse2 + align256(rows * sizeof(float));
+  if (dtype == NEA_BF16) {
+    w.dqacc = end;
+    end += align256(rows * d * sizeof(float));
+  } else {
+    w.qt = end;
+    w.dot = w.qt + align256(rows * d * sizeof(float));
+    w.kt = w.dot + align256(rows * d * sizeof(float));
+    end = w.kt + align256(kvrows * d * sizeof(float));
+  }
+  w.total = end;
   return w;
 }
 
@@ -155,7 +184,7 @@ int nea_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LS
 
 size_t nea_attn_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d, int dtype) {
   if (check_common(B, H, Hkv, N, d, 1.0f, 1, dtype) != NEA_OK) return 0;
-  return ws_layout(B, H, N, d, dtype).total;
+  return ws_layout(B, H, Hkv, N, d, dtype).total;
 }
 
 // Shared by the backward entry points: checks and fills the arguments every
@@ -172,7 +201,7 @@ static int prepare_bwd(BwdArgs* a, const void* Q, const void* K, const void* V, 
     return NEA_ERR_INVALID;
   int st = check_common(B, H, Hkv, N, d, scale, causal, dtype);
   if (st != NEA_OK) return st;
-  const WsLayout w = ws_layout(B, H, N, d, dtype);
+  const WsLayout w = ws_layout(B, H, Hkv, N, d, dtype);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
       workspace_bytes < w.total)
     return NEA_ERR_WORKSPACE;
@@ -180,7 +209,12 @@ static int prepare_bwd(BwdArgs* a, const void* Q, const void* K, const void* V, 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a->delta = reinterpret_cast<float*>(ws + w.delta);
   a->lse2 = reinterpret_cast<float*>(ws + w.lse2);
-  a->dq_acc = dtype == NEA_BF16 ? reinterpret_cast<float*>(ws + w.dqacc) : static_cast<float*>(dQ);
+  a->dq_acc = dtype == NEA_BF16 ? reinterpret_cast<float*>(ws + w.dqacc) : nullptr;
+  if (dtype == NEA_F32) {
+    a->qt = reinterpret_cast<float*>(ws + w.qt);
+    a->dot = reinterpret_cast<float*>(ws + w.dot);
+    a->kt = reinterpret_cast<float*>(ws + w.kt);
+  }
   if (need_maps) {
     const CUtensorMapDataType dt =
         dtype == NEA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
@@ -188,15 +222,33 @@ static int prepare_bwd(BwdArgs* a, const void* Q, const void* K, const void* V, 
     const long long bh = static_cast<long long>(B) * H, bkv = static_cast<long long>(B) * Hkv;
     if (!encode_3d(&a->tmQ, Q, dt, es, d, N, bh) || !encode_3d(&a->tmK, K, dt, es, d, N, bkv) ||
         !encode_3d(&a->tmV, V, dt, es, d, N, bkv) || !encode_3d(&a->tmdO, dO, dt, es, d, N, bh) ||
-        !encode_3d(&a->tmdQacc, a->dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, N, bh))
+        (dtype == NEA_BF16 &&
+         !encode_3d(&a->tmdQacc, a->dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, N, bh)))
       return NEA_ERR_CUDA;
     a->status = status_ptr();
     if (!a->status) return NEA_ERR_CUDA;
   }
-  a->O = O; a->dO = dO; a->lse = LSE; a->dQ = dQ; a->dK = dK; a->dV = dV;
+  a->Q = Q; a->K = K; a->O = O; a->dO = dO; a->lse = LSE; a->dQ = dQ; a->dK = dK; a->dV = dV;
   a->B = B; a->H = H; a->Hkv = Hkv; a->N = N; a->d = d; a->causal = causal;
   a->scale = scale; a->dtype = dtype;
   return NEA_OK;
+}
+
+// The main stage: one kernel for bf16; for fp32, the tf32 transposes of Q,
+// dO and K into the workspace, then the dK/dV and dQ kernels.
+static int run_main(const BwdArgs& a, cudaStream_t s) {
+  if (a.dtype == NEA_BF16)
+    return launch_bwd_main(a, s) == cudaSuccess ? NEA_OK : NEA_ERR_CUDA;
+  const long long bh = static_cast<long long>(a.B) * a.H, bkv = static_cast<long long>(a.B) * a.Hkv;
+  CUtensorMap tmQt, tmdOt, tmKt;
+  if (!encode_3d_t(&tmQt, a.qt, a.d, a.N, bh) || !encode_3d_t(&tmdOt, a.dot, a.d, a.N, bh) ||
+      !encode_3d_t(&tmKt, a.kt, a.d, a.N, bkv))
+    return NEA_ERR_CUDA;
+  if (launch_transpose_f32(static_cast<const float*>(a.Q), a.qt, bh, a.N, s) != cudaSuccess ||
+      launch_transpose_f32(static_cast<const float*>(a.dO), a.dot, bh, a.N, s) != cudaSuccess ||
+      launch_transpose_f32(static_cast<const float*>(a.K), a.kt, bkv, a.N, s) != cudaSuccess)
+    return NEA_ERR_CUDA;
+  return launch_bwd_main_f32(a, tmQt, tmdOt, tmKt, s) == cudaSuccess ? NEA_OK : NEA_ERR_CUDA;
 }
 
 int nea_attn_bwd_preprocess(const void* O, const void* dO, const float* LSE, void* dQ,
@@ -217,8 +269,7 @@ int nea_attn_bwd_main(const void* Q, const void* K, const void* V, const void* d
   int st = prepare_bwd(&a, Q, K, V, nullptr, dO, nullptr, dQ, dK, dV, workspace, workspace_bytes,
                        B, H, Hkv, N, d, scale, causal, dtype, false, true, true);
   if (st != NEA_OK) return st;
-  return launch_bwd_main(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? NEA_OK
-                                                                              : NEA_ERR_CUDA;
+  return run_main(a, static_cast<cudaStream_t>(stream));
 }
 
 int nea_attn_bwd_finalize(void* dQ, void* workspace, size_t workspace_bytes, int B, int H,
@@ -243,7 +294,8 @@ int nea_attn_bwd(const void* Q, const void* K, const void* V, const void* O, con
   if (st != NEA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (launch_bwd_pre(a, s) != cudaSuccess) return NEA_ERR_CUDA;
-  if (launch_bwd_main(a, s) != cudaSuccess) return NEA_ERR_CUDA;
+  st = run_main(a, s);
+  if (st != NEA_OK) return st;
   if (dtype == NEA_BF16 && launch_bwd_post(a, s) != cudaSuccess) return NEA_ERR_CUDA;
   return NEA_OK;
 }

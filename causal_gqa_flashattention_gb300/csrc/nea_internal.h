@@ -23,12 +23,17 @@ struct FwdArgs {
 struct BwdArgs {
   CUtensorMap tmQ, tmK, tmV, tmdO;  // loads, 3-D {d, N, heads}, 128-B swizzle
   CUtensorMap tmdQacc;              // fp32 reduce target {d, N, B*H}, 128-B swizzle
+  const void* Q;                    // [B,H,N,d] dtype
+  const void* K;                    // [B,Hkv,N,d] dtype
   const void* O;                    // [B,H,N,d] dtype
   const void* dO;
   const float* lse;                 // [B*H*N]
   float* delta;                     // workspace: D [B*H*N]
   float* lse2;                      // workspace: LSE * log2(e) [B*H*N]
-  float* dq_acc;                    // fp32 dQ accumulator [B,H,N,d] (== dQ for fp32)
+  float* dq_acc;                    // bf16: fp32 dQ accumulator [B,H,N,d]; fp32: null
+  float* qt;                        // fp32 only: tf32-rounded Q^T  [B*H][d][N]
+  float* dot;                       // fp32 only: tf32-rounded dO^T [B*H][d][N]
+  float* kt;                        // fp32 only: tf32-rounded K^T  [B*Hkv][d][N]
   void* dQ;                         // output
   void* dK;
   void* dV;
@@ -44,5 +49,11 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_post(const BwdArgs& a, cudaStream_t stream);
+// fp32 path: transposes for the workspace, then the dK/dV and dQ kernels.
+cudaError_t launch_transpose_f32(const float* src, float* dst, long long heads, int N,
+                                 cudaStream_t stream);
+cudaError_t launch_bwd_main_f32(const BwdArgs& a, const CUtensorMap& tmQt,
+                                const CUtensorMap& tmdOt, const CUtensorMap& tmKt,
+                                cudaStream_t stream);
 
 }  // namespace nea

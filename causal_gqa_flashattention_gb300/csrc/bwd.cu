@@ -13,7 +13,8 @@
 //            group's query heads and the query tiles i >= j (causal):
 //              warp 0      TMA producer (K_j, V_j once; Q_i, dO_i, L2_i, Ds_i
 //                          per step into a ring)
-//              warp 1      MMA issuer + TMEM owner
+//              warp 1      MMA issuer A (S^T, dP^T, dV) + TMEM owner
+//              warp 2      MMA issuer B (dK, dQ)
 //              warps 4..11 "compute", two warpgroups splitting the 128 query
 //                          columns: thread = key row; P^T = exp2(S^T c - L2)
 //                          to TMEM (bf16), dS^T = P^T o (scale dP^T - Ds) to
@@ -158,13 +159,11 @@ struct BwdCfg {
   static constexpr int OFF_DSR = OFF_L2 + QST * 512;
   static constexpr int SMEM_BYTES = 1024 + OFF_DSR + QST * 512;
   static constexpr int THREADS = 512;
-  // S_{n+1} may be issued before dK_n only when the ring holds two steps.
-  static constexpr bool EARLY_S = QST >= 2;
 };
 
 enum : int {
   C_KVFULL = 0, C_SFULL, C_DPFULL, C_PFULL, C_DSFULL, C_DSEMPTY, C_DQFULL, C_DQFREE, C_FINAL,
-  C_DRAIN, C_QFULL  // then QFULL[QST], DOFULL[QST], QEMPTY[QST]
+  C_DRAIN, C_DRAIN2, C_QFULL  // then QFULL[QST], DOFULL[QST], QEMPTY[QST]
 };
 
 template <int D>
@@ -214,12 +213,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
     mbar_init(bar(C_DSEMPTY), 1);
     mbar_init(bar(C_DQFULL), 1);
     mbar_init(bar(C_DQFREE), 128);
-    mbar_init(bar(C_FINAL), 1);
+    mbar_init(bar(C_FINAL), 2);  // one commit per MMA issuer
     mbar_init(bar(C_DRAIN), 1);
+    mbar_init(bar(C_DRAIN2), 1);
     for (int s = 0; s < QST; ++s) {
       mbar_init(qfull(s), 1);
       mbar_init(dofull(s), 1);
-      mbar_init(qempty(s), 1 + 8);  // MMA commit + one arrive per compute warp
+      mbar_init(qempty(s), 2 + 8);  // one commit per MMA issuer + one arrive per compute warp
     }
     fence_barrier_init();
   }
@@ -283,12 +283,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ MMA issuer A
+    // S, dP and dV.  A tcgen05.mma chain issued by one thread advances at
+    // about one instruction per ~130 cycles whatever N is, so the step's MMAs
+    // are split between two issuing warps: A (here) and B (warp 2: dK, dQ).
+    // Each issuer's tcgen05.commit tracks only its own MMAs; every hazard
+    // between the two goes through an mbarrier.
     if (lane == 0) {
       constexpr uint32_t idS = make_idesc<MmaKind::kBF16>(128, 128, false, false);
       constexpr uint32_t idDV = make_idesc<MmaKind::kBF16>(128, D, false, true);
-      constexpr uint32_t idDK = make_idesc<MmaKind::kBF16>(128, D, false, true);
-      constexpr uint32_t idDQ = make_idesc<MmaKind::kBF16>(128, D, true, true);
       auto issue_s = [&](int n) {  // S^T = K_j Q_i^T
         const int s = n % QST;
 #pragma unroll
@@ -315,10 +318,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
       auto wait_do = [&](int n, uint32_t id) {
         return mbar_wait(dofull(n % QST), (n / QST) & 1, abort, id, status);
       };
-      // Issue order per step n (ring depth 2): dV_n, S_{n+1}, dK_n, dQ_n, dP_{n+1}
-      // so the next step's S and dP run while the compute warps finish step n.
-      // With a ring of depth 1, Q_{n+1} only lands after dK_n, so S_{n+1}
-      // moves behind dK_n.
       bool ok = mbar_wait(bar(C_KVFULL), 0, abort, 22, status) && wait_q(0, 23);
       if (ok) {
         tc_fence_after();
@@ -331,7 +330,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
       }
       for (int n = 0; ok && n < nsteps; ++n) {
         const int s = n % QST;
-        const bool more = n + 1 < nsteps;
         // dV += P^T dO_i
         if (!mbar_wait(bar(C_PFULL), n & 1, abort, 26, status)) break;
         tc_fence_after();
@@ -340,13 +338,36 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
           mma_ts<MmaKind::kBF16>(tmem + C::DV_COL, tmem + C::P_COL + k * 8,
                                  sdesc_sw128(sDO(s) + k * 16 * 128, C::BLK_BYTES, 1024), idDV,
                                  (n > 0 || k > 0) ? 1u : 0u);
-        if (C::EARLY_S && more) {
-          if (!wait_q(n + 1, 23)) break;
-          tc_fence_after();
-          issue_s(n + 1);
-        }
+        mma_commit(qempty(s));  // dO_i no longer read by A
+        if (n + 1 == nsteps) break;
+        // S_{n+1}: the compute warps have read S_n (PFULL_n)
+        if (!wait_q(n + 1, 23)) break;
+        tc_fence_after();
+        issue_s(n + 1);
+        // dP_{n+1}: the compute warps have read dP_n (DSFULL_n); with d = 128
+        // dQ_n shares dP's columns and must have been drained (DQFREE_n)
+        if (!wait_do(n + 1, 24) || !mbar_wait(bar(C_DSFULL), n & 1, abort, 25, status)) break;
+        if (C::DQ_ALIAS_DP && !mbar_wait(bar(C_DQFREE), n & 1, abort, 25, status)) break;
+        tc_fence_after();
+        issue_dp(n + 1);
+      }
+      mma_commit(bar(C_FINAL));
+      mma_commit(bar(C_DRAIN));
+      mbar_wait_drain(bar(C_DRAIN), 0, 29, status);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ MMA issuer B
+    // dK and dQ.
+    if (lane == 0) {
+      constexpr uint32_t idDK = make_idesc<MmaKind::kBF16>(128, D, false, true);
+      constexpr uint32_t idDQ = make_idesc<MmaKind::kBF16>(128, D, true, true);
+      bool ok = mbar_wait(bar(C_KVFULL), 0, abort, 37, status);
+      for (int n = 0; ok && n < nsteps; ++n) {
+        const int s = n % QST;
         // dK += dS^T Q_i
-        if (!mbar_wait(bar(C_DSFULL), n & 1, abort, 27, status)) break;
+        if (!mbar_wait(qfull(s), (n / QST) & 1, abort, 38, status) ||
+            !mbar_wait(bar(C_DSFULL), n & 1, abort, 27, status))
+          break;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < C::NK_T; ++k) {
@@ -355,13 +376,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
                                  sdesc_sw128(sQ(s) + k * 16 * 128, C::BLK_BYTES, 1024), idDK,
                                  (n > 0 || k > 0) ? 1u : 0u);
         }
-        mma_commit(qempty(s));
-        if (!C::EARLY_S && more) {
-          if (!wait_q(n + 1, 23)) break;
-          tc_fence_after();
-          issue_s(n + 1);
-        }
-        // dQ_i = dS K_j
+        mma_commit(qempty(s));  // Q_i no longer read by B
+        // dQ_i = dS K_j (the dQ warps have drained dQ_{n-1} when d = 64)
         if (!C::DQ_ALIAS_DP && n > 0 && !mbar_wait(bar(C_DQFREE), (n - 1) & 1, abort, 28, status))
           break;
         tc_fence_after();
@@ -373,17 +389,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
                                  k > 0 ? 1u : 0u);
         mma_commit(bar(C_DSEMPTY));
         mma_commit(bar(C_DQFULL));
-        if (more) {
-          if (!wait_do(n + 1, 24)) break;
-          // d=128: dP shares its columns with dQ_n, which must be drained first
-          if (C::DQ_ALIAS_DP && !mbar_wait(bar(C_DQFREE), n & 1, abort, 25, status)) break;
-          tc_fence_after();
-          issue_dp(n + 1);
-        }
       }
       mma_commit(bar(C_FINAL));
-      mma_commit(bar(C_DRAIN));
-      mbar_wait_drain(bar(C_DRAIN), 0, 29, status);
+      mma_commit(bar(C_DRAIN2));
+      mbar_wait_drain(bar(C_DRAIN2), 0, 39, status);
     }
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ compute

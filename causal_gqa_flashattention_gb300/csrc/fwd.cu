@@ -52,7 +52,11 @@ struct FwdCfg {
 };
 
 // mbarrier slots
-enum : int { B_QFULL = 0, B_SFULL, B_SFREE, B_PFULL, B_ODONE, B_DRAIN, B_QREADY, B_KFULL };
+// P and O += P V are split in two halves of the key tile (keys 0..63 and
+// 64..127): PFULL1/ODONE1 and PFULL2/ODONE2, so that the first half's MMAs
+// run while the softmax computes the second half.
+enum : int { B_QFULL = 0, B_SFULL, B_SFREE, B_PFULL1, B_PFULL2, B_ODONE1, B_ODONE2, B_DRAIN,
+             B_QREADY, B_KFULL };
 // K_FULL[s] = B_KFULL + s, V_FULL[s] = B_KFULL + ST + s, KV_EMPTY[s] = B_KFULL + 2 ST + s
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -95,8 +99,10 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
     mbar_init(bar(B_QFULL), 1);
     mbar_init(bar(B_SFULL), 1);
     mbar_init(bar(B_SFREE), 128);
-    mbar_init(bar(B_PFULL), 128);
-    mbar_init(bar(B_ODONE), 1);
+    mbar_init(bar(B_PFULL1), 128);
+    mbar_init(bar(B_PFULL2), 128);
+    mbar_init(bar(B_ODONE1), 1);
+    mbar_init(bar(B_ODONE2), 1);
     mbar_init(bar(B_DRAIN), 1);
     for (int s = 0; s < 3 * ST; ++s) mbar_init(bar(B_KFULL + s), 1);
     for (int s = 0; s < 2 * ST; ++s) mbar_init(bar(B_KFULL + 3 * ST + s), 128);
@@ -179,24 +185,32 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
           if (!mbar_wait(bar(B_SFREE), j & 1, abort, 5, status) || !issue_s(j + 1)) break;
         }
         const int s = j % ST;
-        if (!mbar_wait(bar(B_PFULL), j & 1, abort, 6, status)) break;
         const int vbar = C::TRANSPOSE_V ? B_KFULL + 3 * ST + s : B_KFULL + ST + s;
         if (!mbar_wait(bar(vbar), (j / ST) & 1, abort, 7, status)) break;
-        tc_fence_after();
         const uint32_t sV = sKV + (2 * s + 1) * C::TILE_BYTES;
+        bool half_ok = true;
 #pragma unroll
-        for (int k = 0; k < C::NK_PV; ++k) {
-          uint64_t bdesc;
-          if constexpr (C::TRANSPOSE_V)  // V^T K-major: 32-B K-step, 4 per 128-B block
-            bdesc = sdesc_sw128(sVT + s * C::VT_BYTES + (k / 4) * C::VT_BLK_BYTES + (k % 4) * 32,
-                                16, 1024);
-          else  // V MN-major: K-step = KPER rows of 128 B
-            bdesc = sdesc_sw128(sV + k * C::KPER * 128, C::BLK_BYTES, 1024);
-          mma_ts<KIND>(tmem + C::O_COL, tmem + C::P_COL + k * 8, bdesc, idPV,
-                       (j > 0 || k > 0) ? 1u : 0u);
+        for (int hf = 0; hf < 2; ++hf) {
+          if (!mbar_wait(bar(hf == 0 ? B_PFULL1 : B_PFULL2), j & 1, abort, 6, status)) {
+            half_ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int k = hf * C::NK_PV / 2; k < (hf + 1) * C::NK_PV / 2; ++k) {
+            uint64_t bdesc;
+            if constexpr (C::TRANSPOSE_V)  // V^T K-major: 32-B K-step, 4 per 128-B block
+              bdesc = sdesc_sw128(sVT + s * C::VT_BYTES + (k / 4) * C::VT_BLK_BYTES + (k % 4) * 32,
+                                  16, 1024);
+            else  // V MN-major: K-step = KPER rows of 128 B
+              bdesc = sdesc_sw128(sV + k * C::KPER * 128, C::BLK_BYTES, 1024);
+            mma_ts<KIND>(tmem + C::O_COL, tmem + C::P_COL + k * 8, bdesc, idPV,
+                         (j > 0 || k > 0) ? 1u : 0u);
+          }
+          if (hf == 1) mma_commit(bar(B_KFULL + 2 * ST + s));  // stage s free for the producer
+          mma_commit(bar(hf == 0 ? B_ODONE1 : B_ODONE2));
         }
-        mma_commit(bar(B_KFULL + 2 * ST + s));  // stage s free for the producer
-        mma_commit(bar(B_ODONE));
+        if (!half_ok) break;
       }
       // Everything this thread issued must finish before TMEM is freed.
       mma_commit(bar(B_DRAIN));
@@ -307,14 +321,6 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
       }
       const float mx = fmaxf(fmaxf(fmaxf(mv[0], mv[1]), fmaxf(mv[2], mv[3])),
                              fmaxf(fmaxf(mv[4], mv[5]), fmaxf(mv[6], mv[7])));
-      // PV_{j-1} must be complete before P is overwritten or O rescaled.
-      if (j > 0) {
-        if (!mbar_wait_warp(bar(B_ODONE), (j - 1) & 1, abort, 10, status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-      }
       const float m_new = fmaxf(m_ref, mx);
       const bool need = (m_new - m_ref) * c > kRescaleLog2;  // always true on the first tile
       float alpha = 1.f;
@@ -327,49 +333,70 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
       const float2 c2 = make_float2(c, c), moff2 = make_float2(moff, moff);
       float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                        make_float2(0.f, 0.f)};
+      // Two halves of the key tile.  Half h of P may be overwritten once the
+      // half-h MMAs of tile j-1 are done (ODONE_h); O is rescaled only after
+      // both halves of tile j-1 are done and before PFULL1 releases tile j.
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        float p[32];
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float2 x = __ffma2_rn(make_float2(sv[32 * cc + i], sv[32 * cc + i + 1]), c2, moff2);
-          p[i] = ex2(x.x);
-          p[i + 1] = ex2(x.y);
-          rs2[(i >> 1) & 3] = __fadd2_rn(rs2[(i >> 1) & 3], make_float2(p[i], p[i + 1]));
+      for (int hf = 0; hf < 2; ++hf) {
+        if (j > 0) {
+          if (!mbar_wait_warp(bar(hf == 0 ? B_ODONE1 : B_ODONE2), (j - 1) & 1, abort, 10,
+                              status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
         }
-        if constexpr (KIND == MmaKind::kBF16) {
-          uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(p[2 * i], p[2 * i + 1]);
-          tmem_st16(trow + C::P_COL + 16 * cc, pk);
-        } else {
-          uint32_t pk[32];
+        for (int cc = 2 * hf; cc < 2 * hf + 2; ++cc) {
+          float p[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) pk[i] = __float_as_uint(p[i]);
-          tmem_st32(trow + C::P_COL + 32 * cc, pk);
+          for (int i = 0; i < 32; i += 2) {
+            const float2 x =
+                __ffma2_rn(make_float2(sv[32 * cc + i], sv[32 * cc + i + 1]), c2, moff2);
+            p[i] = ex2(x.x);
+            p[i + 1] = ex2(x.y);
+            rs2[(i >> 1) & 3] = __fadd2_rn(rs2[(i >> 1) & 3], make_float2(p[i], p[i + 1]));
+          }
+          if constexpr (KIND == MmaKind::kBF16) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(p[2 * i], p[2 * i + 1]);
+            tmem_st16(trow + C::P_COL + 16 * cc, pk);
+          } else {
+            uint32_t pk[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) pk[i] = __float_as_uint(p[i]);
+            tmem_st32(trow + C::P_COL + 32 * cc, pk);
+          }
         }
+        if (hf == 0 && j > 0 && __any_sync(0xffffffffu, need)) {
+          // O rescale: needs the half-2 MMAs of tile j-1 done as well
+          if (!mbar_wait_warp(bar(B_ODONE2), (j - 1) & 1, abort, 10, status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int cc = 0; cc < D; cc += 32) {
+            uint32_t o[32];
+            tmem_ld32(trow + C::O_COL + cc, o);
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(trow + C::O_COL + cc, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(hf == 0 ? B_PFULL1 : B_PFULL2));
       }
+      if (!ok) break;
       const float2 r01 = __fadd2_rn(rs2[0], rs2[1]), r23 = __fadd2_rn(rs2[2], rs2[3]);
       const float rs = (r01.x + r01.y) + (r23.x + r23.y);
       l = l * alpha + rs;
-      // O rescale after P: the S registers are dead by now
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-#pragma unroll
-        for (int cc = 0; cc < D; cc += 32) {
-          uint32_t o[32];
-          tmem_ld32(trow + C::O_COL + cc, o);
-          tmem_ld_wait(o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(trow + C::O_COL + cc, o);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(B_PFULL));
     }
     // ------------------------------------------------------------ epilogue
-    if (ok) ok = mbar_wait_warp(bar(B_ODONE), (nkv - 1) & 1, abort, 11, status);
+    if (ok) ok = mbar_wait_warp(bar(B_ODONE2), (nkv - 1) & 1, abort, 11, status);
     if (ok) {
       tc_fence_after();
       const float inv = 1.f / l;

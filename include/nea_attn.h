@@ -71,8 +71,10 @@ int nea_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LS
 
 /*
  * Bytes of device workspace nea_attn_bwd() needs for these sizes (256-byte
- * aligned sub-buffers: D [B,H,N] fp32, LSE*log2(e) [B,H,N] fp32 and, for
- * bf16, the fp32 dQ accumulator [B,H,N,d]).  Returns 0 for invalid sizes.
+ * aligned sub-buffers: D [B,H,N] fp32, LSE*log2(e) [B,H,N] fp32, then for
+ * bf16 the fp32 dQ accumulator [B,H,N,d], for fp32 the transposed operands
+ * Q^T, dO^T [B*H][d][N] and K^T [B*Hkv][d][N]).  Returns 0 for invalid or
+ * unsupported sizes.
  */
 size_t nea_attn_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d, int dtype);
 
@@ -80,12 +82,15 @@ size_t nea_attn_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d, int dty
  * Backward.  Given the forward's inputs, its O and LSE, and the upstream
  * gradient dO, writes dQ [B,H,N,d], dK and dV [B,Hkv,N,d] (dtype).
  * Section "Hand-written Backpropagation": the gradient is derived by hand
- * and P is recomputed from LSE instead of stored.  Three kernels run in
- * order on `stream`: a preprocess D = rowsum(dO * O) (which also clears the
- * dQ accumulator), the main kernel (one CTA per 128-row KV tile of one
+ * and P is recomputed from LSE instead of stored.  bf16: three kernels run
+ * in order on `stream`: a preprocess D = rowsum(dO * O) (which also clears
+ * the dQ accumulator), the main kernel (one CTA per 128-row KV tile of one
  * (batch, KV head); dK and dV are summed over the group's query heads in
  * tensor memory, without atomics; dQ partials are added into the fp32
- * accumulator by TMA reductions), and, for bf16, a cast of dQ.
+ * accumulator by TMA reductions), and a cast of dQ.  fp32 (TF32 tensor
+ * cores, whose operands must be K-major): the preprocess, tf32-rounded
+ * transposes of Q, dO and K into the workspace, a dK/dV kernel per KV tile
+ * and a dQ kernel per query tile (each dQ tile written once).
  * `workspace` is a device buffer of at least
  * nea_attn_bwd_workspace_bytes(...) bytes, 256-byte aligned, owned by the
  * caller and not used concurrently by another call; its contents on entry
@@ -112,8 +117,9 @@ int nea_attn_bwd_preprocess(const void* O, const void* dO, const float* LSE, voi
                             int N, int d, float scale, int dtype, void* stream);
 
 /*
- * Stage 2, main kernel: reads Q, K, V, dO and the stage-1 workspace; writes
- * dK, dV and adds every dQ partial into the accumulator.
+ * Stage 2, main kernel(s): reads Q, K, V, dO and the stage-1 workspace;
+ * writes dK, dV and (bf16) adds every dQ partial into the accumulator or
+ * (fp32) writes dQ.
  */
 int nea_attn_bwd_main(const void* Q, const void* K, const void* V, const void* dO, void* dQ,
                       void* dK, void* dV, void* workspace, size_t workspace_bytes, int B, int H,

@@ -101,5 +101,9 @@ def test_workspace_checks(nea):
     assert bwd(nea, ws=0) == -5
     assert bwd(nea, ws=P + 16) == -5          # not 256-byte aligned
     assert bwd(nea, ws_bytes=need - 1) == -5
+    # fp32: D, L2 and the transposed Q, dO, K
+    need32 = nea.bwd_workspace_bytes(2, 12, 4, 1024, 64, 1)
+    assert need32 >= rows * 4 * 2 + 2 * rows * 64 * 4 + 2 * 4 * 1024 * 64 * 4
+    assert nea.bwd_workspace_bytes(2, 12, 4, 1024, 128, 1) == 0   # fp32 supports d = 64 only
     assert nea.bwd_workspace_bytes(2, 12, 5, 1024, 64, 0) == 0
     assert nea.bwd_workspace_bytes(2, 12, 4, 1000, 64, 0) == 0

@@ -180,8 +180,10 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
       bool ok = mbar_wait(bar(C::TRANSPOSE_V ? B_QREADY : B_QFULL), 0, abort, 4, status) &&
                 issue_s(0);
       for (int j = 0; ok && j < nkv; ++j) {
-        if (j + 1 < nkv) {
-          // S_{j+1} overwrites S once the softmax has read S_j.
+        // S_{j+1} overwrites S once the softmax has read S_j.  With a ring of
+        // two stages it is issued before O += P_j V_j; with one stage K_{j+1}
+        // can only land after P_j V_j has freed the stage, so it goes after.
+        if (ST >= 2 && j + 1 < nkv) {
           if (!mbar_wait(bar(B_SFREE), j & 1, abort, 5, status) || !issue_s(j + 1)) break;
         }
         const int s = j % ST;
@@ -211,6 +213,9 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
           mma_commit(bar(hf == 0 ? B_ODONE1 : B_ODONE2));
         }
         if (!half_ok) break;
+        if (ST == 1 && j + 1 < nkv) {
+          if (!mbar_wait(bar(B_SFREE), j & 1, abort, 5, status) || !issue_s(j + 1)) break;
+        }
       }
       // Everything this thread issued must finish before TMEM is freed.
       mma_commit(bar(B_DRAIN));

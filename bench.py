@@ -38,11 +38,18 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+DESCR = {"tiny_f32": "tiny fp32 check shape", "gpt2s_bf16": "GPT-2-small shape",
+         "gpt2s_f32": "GPT-2-small shape, fp32 inputs (TF32)", "long_bf16": "long context",
+         "wide_bf16": "wide head, large logits"}
+
+
 def workload_config(w, extra=None):
-    cfg = {"workload": f"causal GQA attention fwd+bwd, GPT-2-small shape "
+    cfg = {"workload": f"causal GQA attention fwd+bwd, {DESCR.get(w.name, w.name)} "
                        f"B={w.B} H={w.H} Hkv={w.Hkv} N={w.N} d={w.d} {w.dtype}",
            "B": w.B, "H": w.H, "Hkv": w.Hkv, "N": w.N, "d": w.d, "causal": w.causal,
-           "scale": w.scale, "inputs": "seeded synthetic: Q,K,V,dO ~ N(0,1), seed 0",
+           "scale": w.scale,
+           "inputs": f"seeded synthetic (seed 0): Q,K ~ N(0,{w.qk_std:g}^2), V,dO ~ "
+                     f"{'U(-1,1)' if w.vdo == 'uniform' else 'N(0,1)'}",
            "l2": "flushed between timed steps (256 MiB write), outside the step events",
            "parallelism": "replicas"}
     if extra:
@@ -188,13 +195,22 @@ def barrier(ws):
 
 
 def max_over_ranks(x, ws):
+    """Largest value over the ranks (the slowest replica sets the step time).
+    Uses a CUDA tensor under NCCL and a CPU tensor under gloo."""
     if ws == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_value(flops_per_step, ms_step_max, ws):
+    """Whole-job TFLOP/s: every replica runs one step of the workload in
+    parallel, so the job does ws * flops per step, timed by the slowest rank."""
+    return ws * flops_per_step / (ms_step_max * 1e-3) / 1e12
 
 
 def run_cuda(args):
@@ -205,13 +221,14 @@ def run_cuda(args):
     ws, rank, local = dist_setup()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = WORKLOADS[WORKLOAD]
+    w = WORKLOADS[args.workload]
     nea.lib()
     q, k, v, do = make_inputs(w, seed=0, device=dev)
     o = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    wsb = nea.bwd_workspace_bytes(w.B, w.H, w.Hkv, w.N, w.d, nea.NEA_BF16)
+    code = nea.NEA_BF16 if w.dtype == "bf16" else nea.NEA_F32
+    wsb = nea.bwd_workspace_bytes(w.B, w.H, w.Hkv, w.N, w.d, code)
     wsp = torch.empty(wsb, dtype=torch.uint8, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -250,7 +267,7 @@ def run_cuda(args):
     step_ms = [sum(p) for p in per]
     ms_step = max_over_ranks(sum(step_ms) / K, ws)
     flops = w.fwd_flops() + w.bwd_flops()
-    value = ws * flops / (ms_step * 1e-3) / 1e12
+    value = job_value(flops, ms_step, ws)
     k_ms = [sum(p[s] for p in per) / K for s in range(4)]
     peaks, src = load_peaks()
     peak_tc = float(peaks["bf16_tflops"])
@@ -291,14 +308,19 @@ def run_cuda(args):
     main_flops = w.bwd_flops()
     main_tf = main_flops / (k_ms[2] * 1e-3) / 1e12
     rows = w.B * w.H * w.N
-    pre_bytes = 2 * rows * w.d * w.esize + rows * 4 + 2 * rows * 4 + rows * w.d * 4
-    post_bytes = rows * w.d * 4 + rows * w.d * w.esize
+    # bf16: the preprocess also clears the fp32 dQ accumulator and the cast
+    # reads it back; fp32: the dQ kernel writes dQ directly (no cast)
+    acc = rows * w.d * 4 if w.dtype == "bf16" else 0
+    pre_bytes = 2 * rows * w.d * w.esize + rows * 4 + 2 * rows * 4 + acc
+    post_bytes = max(acc + rows * w.d * w.esize if acc else 0, 1)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic", "config": workload_config(w),
         "pct_of_peak": round(100.0 * value / ws / peak_tc, 2),
+        "pct_of_peak_note": "of the dense bf16 tensor peak" + ("" if w.dtype == "bf16" else
+                            "; fp32 inputs run on TF32 tensor cores, whose dense rate is half"),
         "roofline": {"kernel": "bwd_main", "bound": "tensor", "achieved": round(main_tf, 1),
                      "peak": peak_tc, "unit": "TFLOP/s", "frac": round(main_tf / peak_tc, 4),
                      "peak_source": f"bf16_tflops (burst) of {src}",
@@ -313,7 +335,7 @@ def run_cuda(args):
             "bwd_post": {"ms": round(k_ms[3], 5),
                          "gbs": round(post_bytes / (k_ms[3] * 1e-3) / 1e9, 1)},
         },
-        "e2e": {"value": round(ws * flops / (e_ms_step * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        "e2e": {"value": round(job_value(flops, e_ms_step, ws), 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e_ms_step, 4), "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo},
         "gpu_launches": 4 * K,
@@ -322,6 +344,8 @@ def run_cuda(args):
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, seconds=args.cpu_seconds)
+    if w.dtype != "bf16":
+        del line["kernels"]["bwd_post"]
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -362,7 +386,7 @@ def run_reference(args):
         return
     from causal_gqa_flashattention_gb300.workloads import WORKLOADS
     import oracle
-    w = WORKLOADS[WORKLOAD]
+    w = WORKLOADS[args.workload]
     nb = 1
     q, k, v, do = oracle_sample(w, nb)
     flops = (w.fwd_flops() + w.bwd_flops()) * nb / w.B
@@ -397,6 +421,9 @@ def main():
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(
+        ["tiny_f32", "gpt2s_bf16", "gpt2s_f32", "long_bf16", "wide_bf16"]),
+        help="default: the GPT-2-small bf16 shape, the headline measurement")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "cuda":
         args.warmup = 3

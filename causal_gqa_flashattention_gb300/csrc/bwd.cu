@@ -36,9 +36,12 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------- preprocess
-// TPR threads per row, each owning 16 bytes of O and dO; every thread handles
-// kPreRows rows (all loads issued before any use, for memory-level
-// parallelism).
+// Walks the per-head rows padded to whole 128-row tiles (npad = T * 128):
+// padded row p = bh * npad + n.  Real rows (n < N) get Ds = scale * dO.O and
+// L2 = LSE * log2(e); padding rows get Ds = 0 and L2 = +inf, so that the main
+// kernel's exp2(S c - L2) is exactly 0 for them.  TPR threads per row, each
+// owning 16 bytes of O and dO; every thread handles kPreRows rows with all
+// loads issued before any use.
 constexpr int kPreRows = 4;
 
 template <typename T, int D>
@@ -47,19 +50,23 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const T* __restrict__ O,
                                                       const float* __restrict__ lse,
                                                       float* __restrict__ ds_row,
                                                       float* __restrict__ l2_row,
-                                                      float* __restrict__ dq_acc, long long rows,
-                                                      float scale) {
+                                                      float* __restrict__ dq_acc, long long prows,
+                                                      int N, int npad, float scale) {
   constexpr int EPV = 16 / sizeof(T);  // elements per 16-B vector
   constexpr int TPR = D / EPV;         // threads per row
   constexpr int RPB = 256 / TPR;       // rows per block per pass
   const int sub = threadIdx.x % TPR;
-  const long long row0 = static_cast<long long>(blockIdx.x) * RPB * kPreRows + threadIdx.x / TPR;
+  const long long p0 = static_cast<long long>(blockIdx.x) * RPB * kPreRows + threadIdx.x / TPR;
   uint4 ov[kPreRows], gv[kPreRows];
+  long long rrow[kPreRows];  // unpadded row index, or -1 for padding / past the end
 #pragma unroll
   for (int u = 0; u < kPreRows; ++u) {
-    const long long row = row0 + static_cast<long long>(u) * RPB;
-    if (row < rows) {
-      const size_t base = static_cast<size_t>(row) * D + sub * EPV;
+    const long long p = p0 + static_cast<long long>(u) * RPB;
+    const long long bh = p / npad;
+    const int n = static_cast<int>(p - bh * npad);
+    rrow[u] = (p < prows && n < N) ? bh * N + n : -1;
+    if (rrow[u] >= 0) {
+      const size_t base = static_cast<size_t>(rrow[u]) * D + sub * EPV;
       ov[u] = __ldg(reinterpret_cast<const uint4*>(O + base));
       gv[u] = __ldg(reinterpret_cast<const uint4*>(dO + base));
     } else {
@@ -68,7 +75,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const T* __restrict__ O,
   }
 #pragma unroll
   for (int u = 0; u < kPreRows; ++u) {
-    const long long row = row0 + static_cast<long long>(u) * RPB;
+    const long long p = p0 + static_cast<long long>(u) * RPB;
     float acc = 0.f;
     if constexpr (sizeof(T) == 2) {
       const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov[u]);
@@ -85,20 +92,18 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const T* __restrict__ O,
 #pragma unroll
       for (int k = 0; k < 4; ++k) acc = fmaf(o4[k], g4[k], acc);
     }
-    // rows are whole warps' worth (rows % 128 == 0), so the shuffle is safe
+    // every lane of the warp runs the shuffle (padding rows add zeros)
 #pragma unroll
     for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (row < rows) {
-      if (sub == 0) {
-        ds_row[row] = acc * scale;
-        l2_row[row] = lse[row] * kLog2e;
-      }
-      // zero this thread's share of the fp32 accumulator row (D floats)
-      if (dq_acc != nullptr) {
-        float4* z = reinterpret_cast<float4*>(dq_acc + static_cast<size_t>(row) * D);
+    if (p < prows && sub == 0) {
+      ds_row[p] = rrow[u] >= 0 ? acc * scale : 0.f;
+      l2_row[p] = rrow[u] >= 0 ? lse[rrow[u]] * kLog2e : INFINITY;
+    }
+    // zero this thread's share of the fp32 accumulator row (D floats)
+    if (dq_acc != nullptr && rrow[u] >= 0) {
+      float4* z = reinterpret_cast<float4*>(dq_acc + static_cast<size_t>(rrow[u]) * D);
 #pragma unroll
-        for (int k = sub; k < D / 4; k += TPR) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+      for (int k = sub; k < D / 4; k += TPR) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
 }
@@ -178,7 +183,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
   __shared__ int abort_sh;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int T = a.N / kTile;
+  const int T = (a.N + kTile - 1) / kTile;  // the last tile may be partial
   const int BG = a.B * a.Hkv;
   const int G = a.H / a.Hkv;
   const int lin = blockIdx.x;
@@ -263,7 +268,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
         int h, i;
         step_hi(n, h, i);
         const int bh = b * a.H + h;
-        const size_t row0 = static_cast<size_t>(bh) * a.N + static_cast<size_t>(i) * kTile;
+        // per-row terms live in the workspace padded to whole tiles per head
+        const size_t row0 = (static_cast<size_t>(bh) * T + i) * kTile;
         mbar_expect_tx(qfull(s), C::TILE_BYTES + 512);
         for (int k = 0; k < C::NBLK; ++k)
           tma_load_3d(sQ(s) + k * C::BLK_BYTES, &a.tmQ, qfull(s), k * 64, i * kTile, bh);
@@ -423,6 +429,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
       reg_fence(u1);
       const float* l2 = l2_s + s * 128 + q0;
       const bool diag = a.causal && i == j;
+      // A key past N (zero-filled by TMA) must not take part: under the
+      // causal mask it lies after every real query and is masked with the
+      // diagonal; without it, it is masked here.  Padded queries have
+      // L2 = +inf, so their P is already 0.
+      const bool kdead = !a.causal && j * kTile + kr >= a.N;
       uint32_t pk[32];  // P^T row, bf16 pairs (query 2t in the low half)
       auto make_p = [&](const uint32_t (&u)[32], int c0) {
 #pragma unroll
@@ -434,6 +445,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
             if (q0 + c0 + 2 * t < kr) p0 = 0.f;
             if (q0 + c0 + 2 * t + 1 < kr) p1 = 0.f;
           }
+          if (kdead) p0 = p1 = 0.f;
           pk[c0 / 2 + t] = pack_bf16(p0, p1);
         }
       };
@@ -490,6 +502,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
     if (ok) ok = mbar_wait_warp(bar(C_FINAL), 0, abort, 35, status);
     if (ok) {
       tc_fence_after();
+      const bool row_ok = j * kTile + kr < a.N;  // rows past N are not stored
       const size_t row =
           (static_cast<size_t>(b) * a.Hkv + g) * a.N + static_cast<size_t>(j) * kTile + kr;
       __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(half == 0 ? a.dV : a.dK) + row * D;
@@ -506,7 +519,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
           w.y = pack_bf16(__uint_as_float(v[8 * t4 + 2]), __uint_as_float(v[8 * t4 + 3]));
           w.z = pack_bf16(__uint_as_float(v[8 * t4 + 4]), __uint_as_float(v[8 * t4 + 5]));
           w.w = pack_bf16(__uint_as_float(v[8 * t4 + 6]), __uint_as_float(v[8 * t4 + 7]));
-          *reinterpret_cast<uint4*>(dst + cc + 8 * t4) = w;
+          if (row_ok) *reinterpret_cast<uint4*>(dst + cc + 8 * t4) = w;
         }
       }
     }
@@ -575,7 +588,7 @@ cudaError_t launch_main_t(const BwdArgs& a, cudaStream_t stream) {
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const unsigned grid = static_cast<unsigned>(a.B) * a.Hkv * (a.N / kTile);
+  const unsigned grid = static_cast<unsigned>(a.B) * a.Hkv * ((a.N + kTile - 1) / kTile);
   kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(a);
   return cudaGetLastError();
 }
@@ -583,23 +596,24 @@ cudaError_t launch_main_t(const BwdArgs& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t stream) {
-  const long long rows = static_cast<long long>(a.B) * a.H * a.N;
+  const int npad = (a.N + kTile - 1) / kTile * kTile;
+  const long long prows = static_cast<long long>(a.B) * a.H * npad;
   const int esize = a.dtype == 0 ? 2 : 4;
   const int tpr = a.d * esize / 16;
   const long long per_block = static_cast<long long>(256 / tpr) * kPreRows;
-  const unsigned grid = static_cast<unsigned>((rows + per_block - 1) / per_block);
+  const unsigned grid = static_cast<unsigned>((prows + per_block - 1) / per_block);
   if (a.dtype == 0 && a.d == 64)
     bwd_pre_kernel<__nv_bfloat16, 64><<<grid, 256, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(a.O), static_cast<const __nv_bfloat16*>(a.dO), a.lse,
-        a.delta, a.lse2, a.dq_acc, rows, a.scale);
+        a.delta, a.lse2, a.dq_acc, prows, a.N, npad, a.scale);
   else if (a.dtype == 0 && a.d == 128)
     bwd_pre_kernel<__nv_bfloat16, 128><<<grid, 256, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(a.O), static_cast<const __nv_bfloat16*>(a.dO), a.lse,
-        a.delta, a.lse2, a.dq_acc, rows, a.scale);
+        a.delta, a.lse2, a.dq_acc, prows, a.N, npad, a.scale);
   else if (a.dtype == 1 && a.d == 64)
     bwd_pre_kernel<float, 64><<<grid, 256, 0, stream>>>(
         static_cast<const float*>(a.O), static_cast<const float*>(a.dO), a.lse, a.delta, a.lse2,
-        a.dq_acc, rows, a.scale);
+        a.dq_acc, prows, a.N, npad, a.scale);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();

@@ -29,23 +29,26 @@ constexpr int TBLK = D * 128;             // [64 rows][128 B] block of a transpo
 constexpr int TTILE = 4 * TBLK;           // [64 rows][128 fp32]
 
 // ---------------------------------------------------------------- transpose
-// src [heads][N][64] -> dst [heads][64][N], tf32-rounded.  Block = 64 rows of
-// src (one n-range) x all 64 columns, 256 threads.
+// src [heads][N][64] -> dst [heads][64][npad], tf32-rounded, zeros in the
+// columns n >= N (npad = N rounded up to whole 128-row tiles, so that every
+// row of dst starts 16-byte aligned for TMA).  Block = 64 columns n of dst x
+// all 64 rows, 256 threads.
 __global__ void __launch_bounds__(256) transpose_tf32_kernel(const float* __restrict__ src,
-                                                             float* __restrict__ dst, int N) {
+                                                             float* __restrict__ dst, int N,
+                                                             int npad) {
   __shared__ float tile[64][65];
   const int n0 = blockIdx.x * 64;
   const size_t head = blockIdx.y;
   const float* s = src + (head * N + n0) * D;
   for (int e = threadIdx.x; e < 64 * 64; e += 256) {
     const int r = e / 64, c = e % 64;
-    tile[r][c] = s[static_cast<size_t>(r) * D + c];
+    tile[r][c] = n0 + r < N ? s[static_cast<size_t>(r) * D + c] : 0.f;
   }
   __syncthreads();
-  float* d = dst + head * D * N + n0;
+  float* d = dst + head * D * npad + n0;
   for (int e = threadIdx.x; e < 64 * 64; e += 256) {
     const int c = e / 64, r = e % 64;  // write row c of dst, 64 consecutive n
-    d[static_cast<size_t>(c) * N + r] = __uint_as_float(tf32_rna(tile[r][c]));
+    d[static_cast<size_t>(c) * npad + r] = __uint_as_float(tf32_rna(tile[r][c]));
   }
 }
 
@@ -79,7 +82,7 @@ __global__ void __launch_bounds__(DkdvCfg::THREADS, 1)
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int T = a.N / kTile, BG = a.B * a.Hkv, G = a.H / a.Hkv;
+  const int T = (a.N + kTile - 1) / kTile, BG = a.B * a.Hkv, G = a.H / a.Hkv;
   const int j = blockIdx.x / BG, bg = blockIdx.x % BG;
   const int b = bg / a.Hkv, g = bg % a.Hkv;
   const int i0 = a.causal ? j : 0, nI = T - i0, nsteps = G * nI;
@@ -122,7 +125,7 @@ __global__ void __launch_bounds__(DkdvCfg::THREADS, 1)
         int h, i;
         step_hi(n, h, i);
         const int bh = b * a.H + h;
-        const size_t row0 = static_cast<size_t>(bh) * a.N + static_cast<size_t>(i) * kTile;
+        const size_t row0 = (static_cast<size_t>(bh) * T + i) * kTile;  // padded per-row terms
         mbar_expect_tx(bar(F_QFULL), TILE + TTILE + 512);
         for (int k = 0; k < 2; ++k)
           tma_load_3d(base + C::OFF_Q + k * BLK, &a.tmQ, bar(F_QFULL), 32 * k, i * kTile, bh);
@@ -207,12 +210,13 @@ __global__ void __launch_bounds__(DkdvCfg::THREADS, 1)
       tmem_ld_wait(u0);
       reg_fence(u1);
       const bool diag = a.causal && i == j;
+      const bool kdead = !a.causal && j * kTile + kr >= a.N;  // key past N, no causal mask
       float p[64];
 #pragma unroll
       for (int t = 0; t < 64; ++t) {
         const float sv = __uint_as_float(t < 32 ? u0[t] : u1[t - 32]);
         float pv = ex2(fmaf(sv, c, -l2s[t]));
-        if (diag && q0 + t < kr) pv = 0.f;
+        if ((diag && q0 + t < kr) || kdead) pv = 0.f;
         p[t] = pv;
       }
 #pragma unroll
@@ -251,6 +255,7 @@ __global__ void __launch_bounds__(DkdvCfg::THREADS, 1)
     if (ok) ok = mbar_wait_warp(bar(F_FINAL), 0, abort, 52, status);
     if (ok) {
       tc_fence_after();
+      const bool row_ok = j * kTile + kr < a.N;
       const size_t row =
           (static_cast<size_t>(b) * a.Hkv + g) * a.N + static_cast<size_t>(j) * kTile + kr;
       float* dst = static_cast<float*>(half == 0 ? a.dV : a.dK) + row * D;
@@ -262,8 +267,9 @@ __global__ void __launch_bounds__(DkdvCfg::THREADS, 1)
         tmem_ld_wait(v);
 #pragma unroll
         for (int t4 = 0; t4 < 8; ++t4)
-          *reinterpret_cast<uint4*>(dst + cc + 4 * t4) =
-              make_uint4(v[4 * t4], v[4 * t4 + 1], v[4 * t4 + 2], v[4 * t4 + 3]);
+          if (row_ok)
+            *reinterpret_cast<uint4*>(dst + cc + 4 * t4) =
+                make_uint4(v[4 * t4], v[4 * t4 + 1], v[4 * t4 + 2], v[4 * t4 + 3]);
       }
     }
   }
@@ -298,7 +304,7 @@ __global__ void __launch_bounds__(DqCfg::THREADS, 1)
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int T = a.N / kTile, BH = a.B * a.H;
+  const int T = (a.N + kTile - 1) / kTile, BH = a.B * a.H;
   const int it = a.causal ? (T - 1 - blockIdx.x / BH) : (blockIdx.x / BH);  // longest first
   const int bh = blockIdx.x % BH;
   const int b = bh / a.H, h = bh % a.H;
@@ -402,7 +408,9 @@ __global__ void __launch_bounds__(DqCfg::THREADS, 1)
     const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const float c = a.scale * kLog2e;
     const size_t row = static_cast<size_t>(bh) * a.N + static_cast<size_t>(it) * kTile + r;
-    const float l2 = a.lse2[row], dsr = a.delta[row];
+    const size_t prow = (static_cast<size_t>(bh) * T + it) * kTile + r;  // padded per-row terms
+    const float l2 = a.lse2[prow], dsr = a.delta[prow];
+    const bool row_ok = it * kTile + r < a.N;
     bool ok = true;
     for (int jj = 0; jj < nkv; ++jj) {
       if (!mbar_wait_warp(bar(Q_SFULL), jj & 1, abort, 69, status)) {
@@ -416,12 +424,14 @@ __global__ void __launch_bounds__(DqCfg::THREADS, 1)
       tmem_ld_wait(u0);
       reg_fence(u1);
       const bool diag = a.causal && jj == it;
+      // keys past N: masked with the diagonal under the causal mask, here otherwise
+      const int klim = (!a.causal && jj == T - 1) ? a.N - 1 - jj * kTile : kTile;
       float p[64];
 #pragma unroll
       for (int t = 0; t < 64; ++t) {
         const float sv = __uint_as_float(t < 32 ? u0[t] : u1[t - 32]);
         float pv = ex2(fmaf(sv, c, -l2));
-        if (diag && k0 + t > r) pv = 0.f;
+        if ((diag && k0 + t > r) || k0 + t > klim) pv = 0.f;
         p[t] = pv;
       }
       if (!mbar_wait_warp(bar(Q_DPFULL), jj & 1, abort, 70, status)) {
@@ -453,8 +463,9 @@ __global__ void __launch_bounds__(DqCfg::THREADS, 1)
       tmem_ld_wait(v);
 #pragma unroll
       for (int t4 = 0; t4 < 8; ++t4)
-        *reinterpret_cast<uint4*>(dst + 4 * t4) =
-            make_uint4(v[4 * t4], v[4 * t4 + 1], v[4 * t4 + 2], v[4 * t4 + 3]);
+        if (row_ok)
+          *reinterpret_cast<uint4*>(dst + 4 * t4) =
+              make_uint4(v[4 * t4], v[4 * t4 + 1], v[4 * t4 + 2], v[4 * t4 + 3]);
     }
   }
   tc_fence_before();
@@ -470,7 +481,9 @@ __global__ void __launch_bounds__(DqCfg::THREADS, 1)
 
 cudaError_t launch_transpose_f32(const float* src, float* dst, long long heads, int N,
                                  cudaStream_t stream) {
-  transpose_tf32_kernel<<<dim3(N / 64, static_cast<unsigned>(heads)), 256, 0, stream>>>(src, dst, N);
+  const int npad = (N + kTile - 1) / kTile * kTile;
+  transpose_tf32_kernel<<<dim3(npad / 64, static_cast<unsigned>(heads)), 256, 0, stream>>>(
+      src, dst, N, npad);
   return cudaGetLastError();
 }
 
@@ -483,7 +496,7 @@ cudaError_t launch_bwd_main_f32(const BwdArgs& a, const CUtensorMap& tmQt,
   e = cudaFuncSetAttribute(dq_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            DqCfg::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const unsigned T = static_cast<unsigned>(a.N / kTile);
+  const unsigned T = static_cast<unsigned>((a.N + kTile - 1) / kTile);
   dkdv_f32_kernel<<<static_cast<unsigned>(a.B) * a.Hkv * T, DkdvCfg::THREADS, DkdvCfg::SMEM_BYTES,
                     stream>>>(a, tmQt, tmdOt);
   e = cudaGetLastError();

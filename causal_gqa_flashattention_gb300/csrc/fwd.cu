@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
   __shared__ int abort_sh;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int T = a.N / kTile;
+  const int T = (a.N + kTile - 1) / kTile;  // the last tile may be partial
   const int BH = a.B * a.H;
   const int lin = blockIdx.x;
   const int qt = a.causal ? (T - 1 - lin / BH) : (lin / BH);  // longest rows first
@@ -310,10 +310,17 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
         sv[64 + i] = __uint_as_float(u2[i]);
         sv[96 + i] = __uint_as_float(u3[i]);
       }
-      if (a.causal && j == qt) {
+      // Keys past `lim` are masked: above the diagonal on the diagonal tile
+      // (which also covers keys past N under the causal mask: a padded key
+      // lies after every real query), and keys past N on the last tile
+      // otherwise.  TMA fills rows past N with zeros.
+      int lim = kTile - 1;
+      if (a.causal && j == qt) lim = r;
+      else if (!a.causal && j == T - 1) lim = a.N - 1 - j * kTile;
+      if (lim < kTile - 1) {
 #pragma unroll
         for (int i = 0; i < 128; ++i)
-          if (i > r) sv[i] = -INFINITY;
+          if (i > lim) sv[i] = -INFINITY;
       }
       // row max as a tree (8 independent chains), not a 128-long chain
       float mv[8];
@@ -437,7 +444,8 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
           }
         }
       }
-      a.lse[static_cast<size_t>(bh) * a.N + qt * kTile + r] = m_ref * a.scale + logf(l);
+      if (qt * kTile + r < a.N)  // rows past N exist only in smem; TMA clips O
+        a.lse[static_cast<size_t>(bh) * a.N + qt * kTile + r] = m_ref * a.scale + logf(l);
       fence_proxy_async();
     }
     named_bar_sync(1, 128);
@@ -464,7 +472,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const unsigned grid = static_cast<unsigned>(a.B) * a.H * (a.N / kTile);
+  const unsigned grid = static_cast<unsigned>(a.B) * a.H * ((a.N + kTile - 1) / kTile);
   kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(a);
   return cudaGetLastError();
 }

@@ -105,7 +105,6 @@ int check_common(int B, int H, int Hkv, int N, int d, float scale, int causal, i
   const long long bh = static_cast<long long>(B) * H;
   if (bh > (1LL << 24) || N > (1 << 24)) return NEA_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return NEA_ERR_UNSUPPORTED;
-  if (N % kTile != 0) return NEA_ERR_UNSUPPORTED;
   (void)bwd;
   if (dtype == NEA_F32 && d != 64) return NEA_ERR_UNSUPPORTED;
   return NEA_OK;
@@ -117,22 +116,26 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 struct WsLayout {
   size_t delta, lse2, dqacc, qt, dot, kt, total;
 };
+// Per-row terms and the transposed fp32 operands are padded to whole 128-row
+// tiles per head (npad rows); the dQ accumulator is not.
 WsLayout ws_layout(int B, int H, int Hkv, int N, int d, int dtype) {
+  const size_t npad = static_cast<size_t>((N + kTile - 1) / kTile) * kTile;
   const size_t rows = static_cast<size_t>(B) * H * N;
-  const size_t kvrows = static_cast<size_t>(B) * Hkv * N;
+  const size_t prows = static_cast<size_t>(B) * H * npad;
+  const size_t kvprows = static_cast<size_t>(B) * Hkv * npad;
   WsLayout w;
   w.delta = 0;
-  w.lse2 = align256(rows * sizeof(float));
+  w.lse2 = align256(prows * sizeof(float));
   w.dqacc = w.qt = w.dot = w.kt = 0;
-  size_t end = w.lse2 + align256(rows * sizeof(float));
+  size_t end = w.lse2 + align256(prows * sizeof(float));
   if (dtype == NEA_BF16) {
     w.dqacc = end;
     end += align256(rows * d * sizeof(float));
   } else {
     w.qt = end;
-    w.dot = w.qt + align256(rows * d * sizeof(float));
-    w.kt = w.dot + align256(rows * d * sizeof(float));
-    end = w.kt + align256(kvrows * d * sizeof(float));
+    w.dot = w.qt + align256(prows * d * sizeof(float));
+    w.kt = w.dot + align256(prows * d * sizeof(float));
+    end = w.kt + align256(kvprows * d * sizeof(float));
   }
   w.total = end;
   return w;
@@ -240,9 +243,10 @@ static int run_main(const BwdArgs& a, cudaStream_t s) {
   if (a.dtype == NEA_BF16)
     return launch_bwd_main(a, s) == cudaSuccess ? NEA_OK : NEA_ERR_CUDA;
   const long long bh = static_cast<long long>(a.B) * a.H, bkv = static_cast<long long>(a.B) * a.Hkv;
+  const int npad = (a.N + kTile - 1) / kTile * kTile;
   CUtensorMap tmQt, tmdOt, tmKt;
-  if (!encode_3d_t(&tmQt, a.qt, a.d, a.N, bh) || !encode_3d_t(&tmdOt, a.dot, a.d, a.N, bh) ||
-      !encode_3d_t(&tmKt, a.kt, a.d, a.N, bkv))
+  if (!encode_3d_t(&tmQt, a.qt, a.d, npad, bh) || !encode_3d_t(&tmdOt, a.dot, a.d, npad, bh) ||
+      !encode_3d_t(&tmKt, a.kt, a.d, npad, bkv))
     return NEA_ERR_CUDA;
   if (launch_transpose_f32(static_cast<const float*>(a.Q), a.qt, bh, a.N, s) != cudaSuccess ||
       launch_transpose_f32(static_cast<const float*>(a.dO), a.dot, bh, a.N, s) != cudaSuccess ||

@@ -16,8 +16,9 @@
 namespace nea {
 namespace {
 
-// D [rows] + LSE*log2(e) [rows] + fp32 dQ accumulator [rows * d], each
-// rounded up to 256 bytes.  32 MiB covers, e.g., B*H*N = 98304 rows at
+// D [padded rows] + LSE*log2(e) [padded rows] + fp32 dQ accumulator
+// [rows * d], each rounded up to 256 bytes (padded rows: N rounded up to a
+// multiple of 128 per head).  32 MiB covers, e.g., B*H*N = 98304 rows at
 // d = 64 bf16 (25.9 MB).
 constexpr size_t kScratchBytes = size_t(32) << 20;
 constexpr int kMaxDevices = 64;

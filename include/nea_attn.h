@@ -29,7 +29,7 @@
  *   accumulation is fp32; bf16 path: P and dS enter the tensor cores as
  *   bf16; fp32 path: operands enter as TF32.
  *   Supported: d in {64, 128} for bf16, d = 64 for fp32; H % Hkv == 0;
- *   N >= 1 and N % 128 == 0 (ragged N returns NEA_ERR_UNSUPPORTED);
+ *   any N >= 1 (a last, partial 128-row tile is masked inside the kernels);
  *   causal in {0, 1}; scale finite and > 0; B >= 1.
  *   `stream` is a cudaStream_t (NULL = legacy default stream).
  *   The caller owns every buffer.  No entry point allocates device memory.

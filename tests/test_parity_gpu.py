@@ -76,9 +76,11 @@ def run_case(nea, w, seed=0, check_bwd=True):
     rdq, rdk, rdv = oracle.attn_bwd(qc, kc, vc, doc, w.scale, w.causal)
     errs = dict(dq=rel_l2(dq, rdq), dk=rel_l2(dk, rdk), dv=rel_l2(dv, rdv))
     assert max(errs.values()) <= (GRAD_REL if w.dtype == "bf16" else F32_REL), errs
-    # the preprocess row term, against the oracle's D on the same (GPU) O
-    rows = w.B * w.H * w.N
-    ds = ws[: rows * 4].view(torch.float32).cpu().numpy().reshape(w.B, w.H, w.N)
+    # the preprocess row term, against the oracle's D on the same (GPU) O;
+    # the workspace holds it per head padded to whole 128-row tiles
+    npad = -(-w.N // 128) * 128
+    prows = w.B * w.H * npad
+    ds = ws[: prows * 4].view(torch.float32).cpu().numpy().reshape(w.B, w.H, npad)[..., : w.N]
     rD = oracle.rowdot(o.cpu(), doc) * w.scale
     assert float(np.abs(ds - rD).max()) <= 1e-4 * max(1.0, float(np.abs(rD).max()))
     return errs
@@ -96,8 +98,27 @@ SMALL = [
 ]
 
 
+# N not a multiple of the 128-row tile: the last query and key tiles are
+# partial (one row, a tile plus one, mid-tile), causal and full masks.
+RAGGED = [
+    custom(1, 2, 1, 1, 64),
+    custom(1, 3, 1, 100, 64),
+    custom(2, 6, 2, 129, 64),
+    custom(1, 4, 2, 200, 64, causal=False),
+    custom(1, 12, 4, 1000, 64),
+    custom(1, 2, 1, 77, 128),
+    custom(1, 4, 2, 300, 128, causal=False),
+    custom(1, 4, 1, 250, 128, qk_std=2.0),
+]
+
+
 @pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
 def test_small_shapes(nea, w):
+    run_case(nea, w)
+
+
+@pytest.mark.parametrize("w", RAGGED, ids=lambda w: w.name)
+def test_ragged_lengths(nea, w):
     run_case(nea, w)
 
 
@@ -114,6 +135,9 @@ def test_full_size_workloads(nea, name):
 
 @pytest.mark.parametrize("w", [WORKLOADS["tiny_f32"], custom(2, 6, 2, 384, 64, "f32"),
                                custom(1, 4, 2, 256, 64, "f32", causal=False),
+                               custom(1, 3, 1, 100, 64, "f32"),
+                               custom(1, 4, 2, 200, 64, "f32", causal=False),
+                               custom(2, 2, 2, 321, 64, "f32"),
                                WORKLOADS["gpt2s_f32"]], ids=lambda w: w.name)
 def test_f32_forward_backward(nea, w):
     run_case(nea, w)

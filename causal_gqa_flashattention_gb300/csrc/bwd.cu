@@ -55,15 +55,20 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const T* __restrict__ O,
   constexpr int EPV = 16 / sizeof(T);  // elements per 16-B vector
   constexpr int TPR = D / EPV;         // threads per row
   constexpr int RPB = 256 / TPR;       // rows per block per pass
+  static_assert(kTile % (RPB * kPreRows) == 0, "a block's rows must divide a tile");
   const int sub = threadIdx.x % TPR;
-  const long long p0 = static_cast<long long>(blockIdx.x) * RPB * kPreRows + threadIdx.x / TPR;
+  // A block's RPB * kPreRows rows divide npad (a multiple of 128), so the
+  // block lies inside one head: bh and the row offset are block-uniform.
+  const long long pb = static_cast<long long>(blockIdx.x) * RPB * kPreRows;
+  const long long bh = pb / npad;
+  const int nb = static_cast<int>(pb - bh * npad) + threadIdx.x / TPR;
+  const long long p0 = pb + threadIdx.x / TPR;
   uint4 ov[kPreRows], gv[kPreRows];
   long long rrow[kPreRows];  // unpadded row index, or -1 for padding / past the end
 #pragma unroll
   for (int u = 0; u < kPreRows; ++u) {
     const long long p = p0 + static_cast<long long>(u) * RPB;
-    const long long bh = p / npad;
-    const int n = static_cast<int>(p - bh * npad);
+    const int n = nb + u * RPB;
     rrow[u] = (p < prows && n < N) ? bh * N + n : -1;
     if (rrow[u] >= 0) {
       const size_t base = static_cast<size_t>(rrow[u]) * D + sub * EPV;
@@ -600,7 +605,7 @@ cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t stream) {
   const long long prows = static_cast<long long>(a.B) * a.H * npad;
   const int esize = a.dtype == 0 ? 2 : 4;
   const int tpr = a.d * esize / 16;
-  const long long per_block = static_cast<long long>(256 / tpr) * kPreRows;
+  const long long per_block = static_cast<long long>(256 / tpr) * kPreRows;  // divides 128
   const unsigned grid = static_cast<unsigned>((prows + per_block - 1) / per_block);
   if (a.dtype == 0 && a.d == 64)
     bwd_pre_kernel<__nv_bfloat16, 64><<<grid, 256, 0, stream>>>(

@@ -206,3 +206,37 @@ int oracle_rowdot_f64(const double *O, const double *dO, double *D, long rows, i
     }
     return 0;
 }
+
+/*
+ * Rotary position embedding of rows of width d (d even), fp64.
+ *
+ * "NanoEuler: modelo GPT-2 ... en C puro sin PyTorch" and "NanoEuler:
+ * Hand-writing GPT-2 in Pure C/CUDA", FAQ on llm.c: the model uses RoPE, with
+ * no formula given.  Taken here as the original rotary embedding: row r of a
+ * [rows][d] array sits at position n = r % N (rows are [heads][N] flattened);
+ * each pair (x_2i, x_2i+1) is turned by the angle n * theta_i with
+ *     theta_i = base^(-2i/d),   i = 0 .. d/2 - 1,
+ *     y_2i   = x_2i cos(a) - x_2i+1 sin(a)
+ *     y_2i+1 = x_2i sin(a) + x_2i+1 cos(a).
+ * `inverse` turns by -a instead (the transpose of the rotation): applied to
+ * the gradient with respect to the rotated rows it gives the gradient with
+ * respect to the unrotated ones.
+ */
+int oracle_rope_f64(const double *X, double *Y, long rows, int N, int d, double base,
+                    int inverse) {
+    if (rows < 0 || N < 1 || d < 2 || (d & 1) || !(base > 0.0)) return -1;
+    const double sgn = inverse ? -1.0 : 1.0;
+#pragma omp parallel for schedule(static)
+    for (long r = 0; r < rows; ++r) {
+        const double n = (double)(r % N);
+        for (int i = 0; i < d / 2; ++i) {
+            const double theta = pow(base, -2.0 * i / d);
+            const double a = sgn * n * theta;
+            const double c = cos(a), s = sin(a);
+            const double x0 = X[(size_t)r * d + 2 * i], x1 = X[(size_t)r * d + 2 * i + 1];
+            Y[(size_t)r * d + 2 * i] = x0 * c - x1 * s;
+            Y[(size_t)r * d + 2 * i + 1] = x0 * s + x1 * c;
+        }
+    }
+    return 0;
+}

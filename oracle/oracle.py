@@ -8,7 +8,9 @@ Definitions followed ("NanoEuler: Hand-writing GPT-2 in Pure C/CUDA"):
 section "Tiled FlashAttention" (exact softmax attention, computed row by row
 here), "Architecture Deep Dive" (decoder, hence causal), "Build and Run"
 (the config's 12 query / 4 KV heads, hence grouped-query attention) and
-"Hand-written Backpropagation" (the hand-derived backward).
+"Hand-written Backpropagation" (the hand-derived backward); the FAQ that
+compares the project with llm.c names RoPE among its techniques, taken here as
+the original rotary embedding on pairs (2i, 2i+1) (see ``rope``).
 """
 from __future__ import annotations
 
@@ -56,6 +58,9 @@ def _load():
             lib.oracle_attn_bwd_f64.restype = ctypes.c_int
             lib.oracle_rowdot_f64.argtypes = [_dp, _dp, _dp, ctypes.c_long, ctypes.c_int]
             lib.oracle_rowdot_f64.restype = ctypes.c_int
+            lib.oracle_rope_f64.argtypes = [_dp, _dp, ctypes.c_long, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_double, ctypes.c_int]
+            lib.oracle_rope_f64.restype = ctypes.c_int
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -135,3 +140,20 @@ def rowdot(o, do):
     if rc != 0:
         raise ValueError("oracle_rowdot_f64 rejected its arguments")
     return out
+
+
+def rope(x, base: float = 10000.0, inverse: bool = False):
+    """Rotary position embedding of x [..., N, d] in fp64 (d even).
+
+    Pair (x_2i, x_2i+1) of the row at position n is turned by n * theta_i,
+    theta_i = base^(-2i/d); ``inverse`` turns by the opposite angle (the
+    transpose, which maps gradients of the rotated rows back).
+    """
+    x = _f64(x)
+    N, d = x.shape[-2], x.shape[-1]
+    rows = x.size // d
+    y = np.empty_like(x)
+    rc = _load().oracle_rope_f64(_ptr(x), _ptr(y), rows, N, d, float(base), int(bool(inverse)))
+    if rc != 0:
+        raise ValueError("oracle_rope_f64 rejected its arguments")
+    return y

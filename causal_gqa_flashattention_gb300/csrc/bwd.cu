@@ -29,6 +29,7 @@
 //  bwd_post  dQ = bf16(dQ accumulator).
 #include "nea_internal.h"
 #include "ptx.cuh"
+#include "rope.cuh"
 
 namespace nea {
 namespace {
@@ -114,12 +115,15 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const T* __restrict__ O,
 }
 
 // ---------------------------------------------------------------- dQ cast
-// Each thread converts kPostVecs groups of 8 fp32 -> 8 bf16.
+// Each thread converts kPostVecs groups of 8 fp32 -> 8 bf16.  With a RoPE
+// table, the 4 pairs of a group are first turned back by their row's angles.
 constexpr int kPostVecs = 4;
 
 __global__ void __launch_bounds__(256) bwd_post_kernel(const float* __restrict__ acc,
                                                        __nv_bfloat16* __restrict__ dq,
-                                                       long long n8) {
+                                                       long long n8,
+                                                       const float2* __restrict__ cs, int N,
+                                                       int d) {
   const long long i0 = static_cast<long long>(blockIdx.x) * 256 * kPostVecs + threadIdx.x;
   float4 a[kPostVecs], b[kPostVecs];
 #pragma unroll
@@ -128,6 +132,22 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const float* __restrict__
     if (i < n8) {
       a[u] = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i);
       b[u] = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i + 1);
+    }
+  }
+  if (cs != nullptr) {
+#pragma unroll
+    for (int u = 0; u < kPostVecs; ++u) {
+      const long long i = i0 + static_cast<long long>(u) * 256;
+      if (i < n8) {
+        const long long e = 8 * i;  // first element of the group; d % 8 == 0
+        const long long row = e / d;
+        const int col = static_cast<int>(e - row * d);
+        const float2* t = cs + static_cast<size_t>(row % N) * (d / 2) + col / 2;
+        rope_inv(a[u].x, a[u].y, __ldg(t));
+        rope_inv(a[u].z, a[u].w, __ldg(t + 1));
+        rope_inv(b[u].x, b[u].y, __ldg(t + 2));
+        rope_inv(b[u].z, b[u].w, __ldg(t + 3));
+      }
     }
   }
 #pragma unroll
@@ -513,10 +533,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
       __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(half == 0 ? a.dV : a.dK) + row * D;
       const uint32_t col = half == 0 ? C::DV_COL : C::DK_COL;
 #pragma unroll
+      // dK of rotated keys -> dK of the caller's keys (RoPE)
+      const float2* rcs = (half == 1 && row_ok && a.rope_cs != nullptr)
+                              ? a.rope_cs + static_cast<size_t>(j * kTile + kr) * (D / 2)
+                              : nullptr;
       for (int cc = 0; cc < D; cc += 32) {
         uint32_t v[32];
         tmem_ld32(trow + col + cc, v);
         tmem_ld_wait(v);
+        if (rcs != nullptr) {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            float x0 = __uint_as_float(v[2 * t]), x1 = __uint_as_float(v[2 * t + 1]);
+            rope_inv(x0, x1, __ldg(rcs + cc / 2 + t));
+            v[2 * t] = __float_as_uint(x0);
+            v[2 * t + 1] = __float_as_uint(x1);
+          }
+        }
 #pragma unroll
         for (int t4 = 0; t4 < 4; ++t4) {
           uint4 w;
@@ -634,7 +667,7 @@ cudaError_t launch_bwd_post(const BwdArgs& a, cudaStream_t stream) {
   const long long n8 = static_cast<long long>(a.B) * a.H * a.N * a.d / 8;
   const long long per_block = 256LL * kPostVecs;
   bwd_post_kernel<<<static_cast<unsigned>((n8 + per_block - 1) / per_block), 256, 0, stream>>>(
-      a.dq_acc, static_cast<__nv_bfloat16*>(a.dQ), n8);
+      a.dq_acc, static_cast<__nv_bfloat16*>(a.dQ), n8, a.rope_cs, a.N, a.d);
   return cudaGetLastError();
 }
 

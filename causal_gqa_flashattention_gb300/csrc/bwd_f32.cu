@@ -17,6 +17,7 @@
 // accumulator and no reduction.
 #include "nea_internal.h"
 #include "ptx.cuh"
+#include "rope.cuh"
 
 namespace nea {
 namespace {
@@ -260,11 +261,24 @@ __global__ void __launch_bounds__(DkdvCfg::THREADS, 1)
           (static_cast<size_t>(b) * a.Hkv + g) * a.N + static_cast<size_t>(j) * kTile + kr;
       float* dst = static_cast<float*>(half == 0 ? a.dV : a.dK) + row * D;
       const uint32_t col = half == 0 ? C::DV_COL : C::DK_COL;
+      // dK of rotated keys -> dK of the caller's keys (RoPE)
+      const float2* rcs = (half == 1 && row_ok && a.rope_cs != nullptr)
+                              ? a.rope_cs + static_cast<size_t>(j * kTile + kr) * (D / 2)
+                              : nullptr;
 #pragma unroll
       for (int cc = 0; cc < D; cc += 32) {
         uint32_t v[32];
         tmem_ld32(trow + col + cc, v);
         tmem_ld_wait(v);
+        if (rcs != nullptr) {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            float x0 = __uint_as_float(v[2 * t]), x1 = __uint_as_float(v[2 * t + 1]);
+            rope_inv(x0, x1, __ldg(rcs + cc / 2 + t));
+            v[2 * t] = __float_as_uint(x0);
+            v[2 * t + 1] = __float_as_uint(x1);
+          }
+        }
 #pragma unroll
         for (int t4 = 0; t4 < 8; ++t4)
           if (row_ok)
@@ -461,6 +475,16 @@ __global__ void __launch_bounds__(DqCfg::THREADS, 1)
       uint32_t v[32];
       tmem_ld32(trow + C::DQ_COL + 32 * half, v);
       tmem_ld_wait(v);
+      if (row_ok && a.rope_cs != nullptr) {  // dQ of rotated queries -> caller's queries
+        const float2* rcs = a.rope_cs + static_cast<size_t>(it * kTile + r) * (D / 2) + 16 * half;
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          float x0 = __uint_as_float(v[2 * t]), x1 = __uint_as_float(v[2 * t + 1]);
+          rope_inv(x0, x1, __ldg(rcs + t));
+          v[2 * t] = __float_as_uint(x0);
+          v[2 * t + 1] = __float_as_uint(x1);
+        }
+      }
 #pragma unroll
       for (int t4 = 0; t4 < 8; ++t4)
         if (row_ok)

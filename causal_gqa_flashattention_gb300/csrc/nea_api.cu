@@ -304,6 +304,49 @@ int nea_attn_bwd(const void* Q, const void* K, const void* V, const void* O, con
   return NEA_OK;
 }
 
+int nea_rope_table(float* cos_sin, int N, int d, double base, void* stream) {
+  if (!cos_sin || (reinterpret_cast<uintptr_t>(cos_sin) & 7u) != 0) return NEA_ERR_INVALID;
+  if (N < 1 || N > (1 << 24) || d < 2 || d > 4096 || (d & 1) || !std::isfinite(base) ||
+      !(base > 0.0))
+    return NEA_ERR_INVALID;
+  return launch_rope_table(reinterpret_cast<float2*>(cos_sin), N, d, base,
+                           static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? NEA_OK
+             : NEA_ERR_CUDA;
+}
+
+int nea_rope_qk(const void* Q, const void* K, void* Qr, void* Kr, const float* cos_sin, int B,
+                int H, int Hkv, int N, int d, int dtype, void* stream) {
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(Qr) || !aligned16(Kr) || !aligned16(cos_sin))
+    return NEA_ERR_INVALID;
+  int st = check_common(B, H, Hkv, N, d, 1.0f, 1, dtype, /*bwd=*/false);
+  if (st != NEA_OK) return st;
+  const long long qrows = static_cast<long long>(B) * H * N;
+  const long long krows = static_cast<long long>(B) * Hkv * N;
+  return launch_rope_rotate(Q, K, Qr, Kr, reinterpret_cast<const float2*>(cos_sin), qrows, krows,
+                            N, d, dtype, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? NEA_OK
+             : NEA_ERR_CUDA;
+}
+
+int nea_attn_bwd_rope(const void* Qr, const void* Kr, const void* V, const void* O,
+                      const void* dO, const float* LSE, const float* cos_sin, void* dQ, void* dK,
+                      void* dV, void* workspace, size_t workspace_bytes, int B, int H, int Hkv,
+                      int N, int d, float scale, int causal, int dtype, void* stream) {
+  if (!aligned16(cos_sin)) return NEA_ERR_INVALID;
+  BwdArgs a;
+  int st = prepare_bwd(&a, Qr, Kr, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes, B, H,
+                       Hkv, N, d, scale, causal, dtype, true, true, true);
+  if (st != NEA_OK) return st;
+  a.rope_cs = reinterpret_cast<const float2*>(cos_sin);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_bwd_pre(a, s) != cudaSuccess) return NEA_ERR_CUDA;
+  st = run_main(a, s);
+  if (st != NEA_OK) return st;
+  if (dtype == NEA_BF16 && launch_bwd_post(a, s) != cudaSuccess) return NEA_ERR_CUDA;
+  return NEA_OK;
+}
+
 int nea_attn_check_status(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return NEA_ERR_CUDA;

@@ -37,6 +37,8 @@ struct BwdArgs {
   void* dQ;                         // output
   void* dK;
   void* dV;
+  const float2* rope_cs;            // null, or RoPE (cos, sin) [N][d/2]: dQ, dK are mapped
+                                    // back through the inverse rotation before they are stored
   unsigned int* status;
   int B, H, Hkv, N, d, causal;
   float scale;
@@ -55,5 +57,10 @@ cudaError_t launch_transpose_f32(const float* src, float* dst, long long heads, 
 cudaError_t launch_bwd_main_f32(const BwdArgs& a, const CUtensorMap& tmQt,
                                 const CUtensorMap& tmdOt, const CUtensorMap& tmKt,
                                 cudaStream_t stream);
+// Rotary embedding: the (cos, sin) table [N][d/2], and Qr = R(Q), Kr = R(K).
+cudaError_t launch_rope_table(float2* cs, int N, int d, double base, cudaStream_t stream);
+cudaError_t launch_rope_rotate(const void* Q, const void* K, void* Qr, void* Kr,
+                               const float2* cs, long long qrows, long long krows, int N, int d,
+                               int dtype, cudaStream_t stream);
 
 }  // namespace nea

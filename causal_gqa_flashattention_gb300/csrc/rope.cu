@@ -1,0 +1,128 @@
+// rope.cu -- rotary position embedding of Q and K rows.
+//
+// The pages name RoPE among the model's techniques ("NanoEuler: Hand-writing
+// GPT-2 in Pure C/CUDA", FAQ on llm.c) without a formula; this is the
+// original rotary embedding: the pair (x_2i, x_2i+1) of the row at position
+// n turns by n * theta_i, theta_i = base^(-2i/d).
+//
+//  rope_table   cs[n][i] = (cos, sin)(n * theta_i), angles in fp64, stored
+//               as fp32 pairs [N][d/2];
+//  rope_rotate  Qr = R(Q), Kr = R(K) in one launch, one 16-byte chunk of a
+//               row per thread (fp32 arithmetic, one rounding to the dtype).
+// The attention kernels then run on Qr and Kr unchanged; the backward maps
+// dQr, dKr back with the transposed rotation in its own epilogues.
+#include <cuda_bf16.h>
+
+#include "nea_internal.h"
+
+namespace nea {
+namespace {
+
+__global__ void __launch_bounds__(256) rope_table_kernel(float2* __restrict__ cs, int N, int half,
+                                                         double base) {
+  const long long idx = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
+  if (idx >= static_cast<long long>(N) * half) return;
+  const int n = static_cast<int>(idx / half), i = static_cast<int>(idx % half);
+  const double theta = pow(base, -2.0 * i / (2.0 * half));
+  double s, c;
+  sincos(static_cast<double>(n) * theta, &s, &c);
+  cs[idx] = make_float2(static_cast<float>(c), static_cast<float>(s));
+}
+
+template <typename T>
+struct Chunk;  // 16 bytes of a row as fp32 values
+template <>
+struct Chunk<__nv_bfloat16> {
+  static constexpr int E = 8;
+  __device__ static void load(const __nv_bfloat16* p, float* v) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      v[2 * k] = __uint_as_float(w[k] << 16);
+      v[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+    }
+  }
+  __device__ static void store(__nv_bfloat16* p, const float* v) {
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+      w[k] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+template <>
+struct Chunk<float> {
+  static constexpr int E = 4;
+  __device__ static void load(const float* p, float* v) {
+    const float4 u = *reinterpret_cast<const float4*>(p);
+    v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+  }
+  __device__ static void store(float* p, const float* v) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+};
+
+// Chunks [0, n0) belong to (x0 -> y0), chunks [n0, n0 + n1) to (x1 -> y1).
+template <typename T>
+__global__ void __launch_bounds__(256) rope_rotate_kernel(const T* __restrict__ x0, T* y0,
+                                                          long long n0, const T* __restrict__ x1,
+                                                          T* y1, long long n1,
+                                                          const float2* __restrict__ cs, int N,
+                                                          int d) {
+  constexpr int E = Chunk<T>::E;
+  long long c = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
+  const T* x = x0;
+  T* y = y0;
+  if (c >= n0) {
+    c -= n0;
+    if (c >= n1) return;
+    x = x1;
+    y = y1;
+  }
+  const int cpr = d / E;  // chunks per row
+  const long long row = c / cpr;
+  const int col = static_cast<int>(c - row * cpr) * E;
+  const int n = static_cast<int>(row % N);
+  const float2* t = cs + static_cast<size_t>(n) * (d / 2) + col / 2;
+  float v[E];
+  Chunk<T>::load(x + c * E, v);
+#pragma unroll
+  for (int k = 0; k < E / 2; ++k) {
+    const float2 r = __ldg(t + k);
+    const float a = v[2 * k], b = v[2 * k + 1];
+    v[2 * k] = fmaf(a, r.x, -(b * r.y));
+    v[2 * k + 1] = fmaf(a, r.y, b * r.x);
+  }
+  Chunk<T>::store(y + c * E, v);
+}
+
+}  // namespace
+
+cudaError_t launch_rope_table(float2* cs, int N, int d, double base, cudaStream_t stream) {
+  const long long n = static_cast<long long>(N) * (d / 2);
+  rope_table_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(cs, N, d / 2,
+                                                                                 base);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_rotate(const void* Q, const void* K, void* Qr, void* Kr,
+                               const float2* cs, long long qrows, long long krows, int N, int d,
+                               int dtype, cudaStream_t stream) {
+  const int E = dtype == 0 ? 8 : 4;
+  const long long n0 = qrows * (d / E), n1 = krows * (d / E);
+  const unsigned grid = static_cast<unsigned>((n0 + n1 + 255) / 256);
+  if (dtype == 0)
+    rope_rotate_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(Q), static_cast<__nv_bfloat16*>(Qr), n0,
+        static_cast<const __nv_bfloat16*>(K), static_cast<__nv_bfloat16*>(Kr), n1, cs, N, d);
+  else
+    rope_rotate_kernel<float><<<grid, 256, 0, stream>>>(
+        static_cast<const float*>(Q), static_cast<float*>(Qr), n0, static_cast<const float*>(K),
+        static_cast<float*>(Kr), n1, cs, N, d);
+  return cudaGetLastError();
+}
+
+}  // namespace nea

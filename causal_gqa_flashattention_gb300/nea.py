@@ -63,6 +63,13 @@ def lib():
             L.nea_attn_bwd_main.restype = _i
             L.nea_attn_bwd_finalize.argtypes = [_vp] * 2 + [ctypes.c_size_t] + [_i] * 6 + [_vp]
             L.nea_attn_bwd_finalize.restype = _i
+            L.nea_rope_table.argtypes = [_vp, _i, _i, ctypes.c_double, _vp]
+            L.nea_rope_table.restype = _i
+            L.nea_rope_qk.argtypes = [_vp] * 5 + [_i] * 6 + [_vp]
+            L.nea_rope_qk.restype = _i
+            L.nea_attn_bwd_rope.argtypes = [_vp] * 11 + [ctypes.c_size_t] + [_i] * 5 + [
+                _f, _i, _i, _vp]
+            L.nea_attn_bwd_rope.restype = _i
             L.nea_attn_check_status.argtypes = [_vp]
             L.nea_attn_check_status.restype = _i
             L.nea_status_string.argtypes = [_i]
@@ -123,9 +130,36 @@ def bwd_workspace_bytes(B, H, Hkv, N, d, dtype=NEA_BF16) -> int:
     return int(lib().nea_attn_bwd_workspace_bytes(B, H, Hkv, N, d, dtype))
 
 
+def rope_table(N, d, *, base=10000.0, device=None, out=None, stream=None):
+    """RoPE (cos, sin) table [N, d/2, 2] fp32 for positions 0..N-1, computed on the GPU."""
+    cs = out if out is not None else torch.empty((N, d // 2, 2), dtype=torch.float32,
+                                                 device=device or "cuda")
+    st = lib().nea_rope_table(_ptr(cs), int(N), int(d), float(base),
+                              ctypes.c_void_p(_stream_handle(stream)))
+    if st != NEA_OK:
+        raise NeaError(st, "nea_rope_table")
+    return cs
+
+
+def rope_qk(q, k, cos_sin, *, qr=None, kr=None, stream=None):
+    """Qr, Kr = R(q), R(k): the rotary embedding of q [B,H,N,d] and k [B,Hkv,N,d]."""
+    B, H, Hkv, N, d = _check(q, k, k)
+    qr = torch.empty_like(q) if qr is None else qr
+    kr = torch.empty_like(k) if kr is None else kr
+    st = lib().nea_rope_qk(_ptr(q), _ptr(k), _ptr(qr), _ptr(kr), _ptr(cos_sin), B, H, Hkv, N, d,
+                           _dtype_code(q), ctypes.c_void_p(_stream_handle(stream)))
+    if st != NEA_OK:
+        raise NeaError(st, "nea_rope_qk")
+    return qr, kr
+
+
 def attn_bwd(q, k, v, o, do, lse, *, causal=True, scale=None, dq=None, dk=None, dv=None,
-             workspace=None, stream=None):
-    """dQ, dK, dV for upstream gradient ``do``, using the forward's O and LSE."""
+             workspace=None, stream=None, rope_cs=None):
+    """dQ, dK, dV for upstream gradient ``do``, using the forward's O and LSE.
+
+    With ``rope_cs`` (the table ``q`` and ``k`` were rotated with), ``q`` and
+    ``k`` are the rotated inputs and dQ, dK are returned with respect to the
+    unrotated ones."""
     B, H, Hkv, N, d = _check(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     code = _dtype_code(q)
@@ -135,12 +169,21 @@ def attn_bwd(q, k, v, o, do, lse, *, causal=True, scale=None, dq=None, dk=None, 
     need = bwd_workspace_bytes(B, H, Hkv, N, d, code)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-    st = lib().nea_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
-                            _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(), B, H, Hkv, N,
-                            d, scale, int(bool(causal)), code,
-                            ctypes.c_void_p(_stream_handle(stream)))
+    if rope_cs is None:
+        st = lib().nea_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                                _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(), B, H,
+                                Hkv, N, d, scale, int(bool(causal)), code,
+                                ctypes.c_void_p(_stream_handle(stream)))
+        what = "nea_attn_bwd"
+    else:
+        st = lib().nea_attn_bwd_rope(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
+                                     _ptr(rope_cs), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                                     workspace.numel(), B, H, Hkv, N, d, scale,
+                                     int(bool(causal)), code,
+                                     ctypes.c_void_p(_stream_handle(stream)))
+        what = "nea_attn_bwd_rope"
     if st != NEA_OK:
-        raise NeaError(st, "nea_attn_bwd")
+        raise NeaError(st, what)
     return dq, dk, dv
 
 

@@ -71,9 +71,10 @@ int nea_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LS
 
 /*
  * Bytes of device workspace nea_attn_bwd() needs for these sizes (256-byte
- * aligned sub-buffers: D [B,H,N] fp32, LSE*log2(e) [B,H,N] fp32, then for
- * bf16 the fp32 dQ accumulator [B,H,N,d], for fp32 the transposed operands
- * Q^T, dO^T [B*H][d][N] and K^T [B*Hkv][d][N]).  Returns 0 for invalid or
+ * aligned sub-buffers, with Npad = N rounded up to a multiple of 128:
+ * D [B*H][Npad] fp32, LSE*log2(e) [B*H][Npad] fp32, then for bf16 the fp32
+ * dQ accumulator [B,H,N,d], for fp32 the transposed operands Q^T, dO^T
+ * [B*H][d][Npad] and K^T [B*Hkv][d][Npad]).  Returns 0 for invalid or
  * unsupported sizes.
  */
 size_t nea_attn_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d, int dtype);
@@ -159,6 +160,49 @@ int nea_attn_bwd_noalloc(const void* Q, const void* K, const void* V, const void
 
 /* Size in bytes of the scratch array behind nea_attn_bwd_noalloc(). */
 size_t nea_attn_bwd_noalloc_max_bytes(void);
+
+/*
+ * Rotary position embedding (RoPE).  The pages name RoPE among the model's
+ * techniques ("NanoEuler: Hand-writing GPT-2 in Pure C/CUDA", FAQ on llm.c)
+ * without a formula; these calls implement the original rotary embedding:
+ * the pair (x_2i, x_2i+1) of the row at position n (n = row index within its
+ * head, 0 .. N-1) turns by the angle n * theta_i, theta_i = base^(-2i/d):
+ *   y_2i = x_2i cos - x_2i+1 sin,   y_2i+1 = x_2i sin + x_2i+1 cos.
+ * Use: build the table once per (N, d, base); rotate Q and K into Qr, Kr;
+ * run nea_attn_fwd() on (Qr, Kr, V); for the gradients call
+ * nea_attn_bwd_rope(), which returns dQ and dK with respect to the
+ * caller's unrotated Q and K.
+ */
+
+/*
+ * Writes cos_sin [N][d/2][2] fp32 (cos, sin of n * theta_i, computed in
+ * fp64).  cos_sin: device pointer, 8-byte aligned, N*d*4 bytes, owned by the
+ * caller.  d even and >= 2, N >= 1, base finite and > 0, else
+ * NEA_ERR_INVALID.  Asynchronous on `stream`.
+ */
+int nea_rope_table(float* cos_sin, int N, int d, double base, void* stream);
+
+/*
+ * Qr = R(Q), Kr = R(K) for Q [B,H,N,d], K [B,Hkv,N,d] (dtype), rotated in
+ * fp32 and rounded once to the dtype.  Qr/Kr may alias Q/K (in place).  All
+ * pointers 16-byte aligned device pointers; cos_sin from nea_rope_table()
+ * for the same N and d.  Shape rules as for nea_attn_fwd().
+ */
+int nea_rope_qk(const void* Q, const void* K, void* Qr, void* Kr, const float* cos_sin, int B,
+                int H, int Hkv, int N, int d, int dtype, void* stream);
+
+/*
+ * Backward of attention on rotated inputs.  Arguments as nea_attn_bwd(),
+ * with Qr, Kr the rotated Q and K the forward ran on, and cos_sin the table
+ * they were rotated with.  dV is as nea_attn_bwd() gives it; dQ and dK are
+ * the gradients with respect to the unrotated Q and K: the kernels apply
+ * the transposed rotation to dQ (in the dQ cast, or the fp32 dQ kernel's
+ * store) and to dK (in the main kernel's store), with no extra pass.
+ */
+int nea_attn_bwd_rope(const void* Qr, const void* Kr, const void* V, const void* O,
+                      const void* dO, const float* LSE, const float* cos_sin, void* dQ, void* dK,
+                      void* dV, void* workspace, size_t workspace_bytes, int B, int H, int Hkv,
+                      int N, int d, float scale, int causal, int dtype, void* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the library's device status

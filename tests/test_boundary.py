@@ -28,7 +28,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("nea_attn_fwd", "nea_attn_bwd", "nea_attn_bwd_workspace_bytes",
-              "nea_attn_check_status", "nea_status_string", "nea_version"):
+              "nea_attn_check_status", "nea_status_string", "nea_version",
+              "nea_rope_table", "nea_rope_qk", "nea_attn_bwd_rope"):
         assert n in names
 
 
@@ -110,3 +111,24 @@ def test_workspace_checks(nea):
     need_r = nea.bwd_workspace_bytes(2, 12, 4, 1000, 64, 0)
     assert need_r >= 2 * (2 * 12 * 1024 * 4) + 2 * 12 * 1000 * 64 * 4
     assert need_r <= need
+
+
+def test_rope_argument_checks(nea):
+    """Host-side validation of the RoPE calls: rejected before any launch."""
+    L = nea.lib()
+    vp = ctypes.c_void_p
+    assert L.nea_rope_table(vp(0), 128, 64, 10000.0, None) == -1          # null
+    assert L.nea_rope_table(vp(P + 4), 128, 64, 10000.0, None) == -1      # misaligned
+    assert L.nea_rope_table(vp(P), 128, 63, 10000.0, None) == -1          # odd d
+    assert L.nea_rope_table(vp(P), 0, 64, 10000.0, None) == -1            # N < 1
+    assert L.nea_rope_table(vp(P), 128, 64, 0.0, None) == -1              # base <= 0
+    assert L.nea_rope_table(vp(P), 128, 64, float("nan"), None) == -1
+    a = GOOD
+    args = lambda ptrs, **kw: [vp(x) for x in ptrs] + [dict(a, **kw)[n] for n in
+                                                      ("B", "H", "Hkv", "N", "d", "dtype")] + [None]
+    assert L.nea_rope_qk(*args([P, P, P, P, 0])) == -1                     # null table
+    assert L.nea_rope_qk(*args([P, P, P + 8, P, P])) == -1                 # misaligned Qr
+    assert L.nea_rope_qk(*args([P] * 5, H=12, Hkv=5)) == -1                # bad group
+    assert L.nea_rope_qk(*args([P] * 5, d=96)) == -2                       # unsupported d
+    bw = [vp(P)] * 6 + [vp(0)] + [vp(P)] * 4
+    assert L.nea_attn_bwd_rope(*bw, 1 << 40, 2, 12, 4, 1024, 64, 0.125, 1, 0, None) == -1

@@ -240,3 +240,65 @@ int oracle_rope_f64(const double *X, double *Y, long rows, int N, int d, double 
     }
     return 0;
 }
+
+/*
+ * Decode attention over a key/value cache, fp64 (the inference use the pages
+ * mention: "NanoEuler: Hand-writing GPT-2 in Pure C/CUDA", FAQ on production
+ * inference -- inference works, without paged or batched caches).
+ *
+ * Reading taken: batch element b holds a contiguous cache of L_b = lens[b]
+ * rows (1 <= L_b <= Lmax) that already includes the nq new tokens, so new
+ * token t (0 <= t < nq, nq <= L_b) sits at position L_b - nq + t and, under
+ * the decoder's causal mask, sees cache rows 0 .. L_b - nq + t.  Query head h
+ * reads KV head h / (H / Hkv).  Row by row, the plain softmax:
+ *     S_j = scale * q . k_j,  O = sum_j softmax(S)_j v_j,  LSE = ln sum_j e^S_j
+ * Layouts: Q, O [B][H][nq][d]; Kc, Vc [B][Hkv][Lmax][d]; LSE [B][H][nq].
+ */
+int oracle_attn_decode_f64(const double *Q, const double *Kc, const double *Vc, const int *lens,
+                           double *O, double *LSE, int B, int H, int Hkv, int nq, int Lmax,
+                           int d, double scale) {
+    if (B < 1 || H < 1 || Hkv < 1 || nq < 1 || Lmax < 1 || d < 1 || H % Hkv) return -1;
+    for (int b = 0; b < B; ++b)
+        if (lens[b] < nq || lens[b] > Lmax) return -1;
+    const int G = H / Hkv;
+    int err = 0;
+#pragma omp parallel
+    {
+        double *p = (double *)malloc(sizeof(double) * (size_t)Lmax);
+        if (!p) {
+#pragma omp atomic write
+            err = 1;
+        }
+#pragma omp for collapse(2) schedule(dynamic)
+        for (int b = 0; b < B; ++b)
+            for (int h = 0; h < H; ++h) {
+                if (!p) continue;
+                const int g = h / G, L = lens[b];
+                const double *K = Kc + ((size_t)b * Hkv + g) * Lmax * d;
+                const double *V = Vc + ((size_t)b * Hkv + g) * Lmax * d;
+                for (int t = 0; t < nq; ++t) {
+                    const double *q = Q + (((size_t)b * H + h) * nq + t) * d;
+                    const int len = L - nq + t + 1;
+                    double m = -INFINITY;
+                    for (int j = 0; j < len; ++j) {
+                        double s = 0.0;
+                        for (int k = 0; k < d; ++k) s += q[k] * K[(size_t)j * d + k];
+                        p[j] = scale * s;
+                        if (p[j] > m) m = p[j];
+                    }
+                    double l = 0.0;
+                    for (int j = 0; j < len; ++j) {
+                        p[j] = exp(p[j] - m);
+                        l += p[j];
+                    }
+                    double *o = O + (((size_t)b * H + h) * nq + t) * d;
+                    for (int k = 0; k < d; ++k) o[k] = 0.0;
+                    for (int j = 0; j < len; ++j)
+                        for (int k = 0; k < d; ++k) o[k] += p[j] / l * V[(size_t)j * d + k];
+                    LSE[((size_t)b * H + h) * nq + t] = m + log(l);
+                }
+            }
+        free(p);
+    }
+    return err ? -1 : 0;
+}

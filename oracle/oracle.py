@@ -10,7 +10,9 @@ here), "Architecture Deep Dive" (decoder, hence causal), "Build and Run"
 (the config's 12 query / 4 KV heads, hence grouped-query attention) and
 "Hand-written Backpropagation" (the hand-derived backward); the FAQ that
 compares the project with llm.c names RoPE among its techniques, taken here as
-the original rotary embedding on pairs (2i, 2i+1) (see ``rope``).
+the original rotary embedding on pairs (2i, 2i+1) (see ``rope``); the FAQ on
+production inference says inference works (see ``attn_decode`` for the
+cache reading taken).
 """
 from __future__ import annotations
 
@@ -61,6 +63,10 @@ def _load():
             lib.oracle_rope_f64.argtypes = [_dp, _dp, ctypes.c_long, ctypes.c_int, ctypes.c_int,
                                             ctypes.c_double, ctypes.c_int]
             lib.oracle_rope_f64.restype = ctypes.c_int
+            lib.oracle_attn_decode_f64.argtypes = [_dp, _dp, _dp, ctypes.POINTER(ctypes.c_int),
+                                                   _dp, _dp] + [ctypes.c_int] * 6 + [
+                                                       ctypes.c_double]
+            lib.oracle_attn_decode_f64.restype = ctypes.c_int
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -157,3 +163,23 @@ def rope(x, base: float = 10000.0, inverse: bool = False):
     if rc != 0:
         raise ValueError("oracle_rope_f64 rejected its arguments")
     return y
+
+
+def attn_decode(q, k_cache, v_cache, lens, scale: float):
+    """Decode attention: q [B,H,nq,d] (the nq newest tokens), caches
+    [B,Hkv,Lmax,d] holding lens[b] valid rows that include the new tokens.
+    New token t of batch b sits at position lens[b] - nq + t and sees cache
+    rows up to it.  Returns (O [B,H,nq,d], LSE [B,H,nq]) in fp64."""
+    q, kc, vc = _f64(q), _f64(k_cache), _f64(v_cache)
+    B, H, nq, d = q.shape
+    Hkv, Lmax = kc.shape[1], kc.shape[2]
+    assert kc.shape == (B, Hkv, Lmax, d) and vc.shape == kc.shape
+    ln = np.ascontiguousarray(np.asarray(lens, dtype=np.int32).reshape(B))
+    o = np.empty_like(q)
+    lse = np.empty((B, H, nq), dtype=np.float64)
+    rc = _load().oracle_attn_decode_f64(_ptr(q), _ptr(kc), _ptr(vc),
+                                        ln.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), _ptr(o),
+                                        _ptr(lse), B, H, Hkv, nq, Lmax, d, float(scale))
+    if rc != 0:
+        raise ValueError("oracle_attn_decode_f64 rejected its arguments")
+    return o, lse

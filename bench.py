@@ -348,6 +348,9 @@ def run_cuda(args):
         "clocks": clk.summary(),
         "wall_s_timed_region": round(wall, 4),
     }
+    if not args.no_extras and w.dtype == "bf16":
+        line["extras"] = measure_extras(nea, w, q, k, v, do, o, lse, wsp, l2_flush, stream,
+                                        peak_hbm, src, reps=max(10, min(K, 50)))
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, seconds=args.cpu_seconds)
     if w.dtype != "bf16":
@@ -357,6 +360,68 @@ def run_cuda(args):
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def _time_ms(fn, l2_flush, stream, reps):
+    """Mean device time of fn() over reps calls, L2 flushed before each."""
+    import torch
+    for _ in range(3):
+        l2_flush()
+        fn()
+    ts = []
+    for _ in range(reps):
+        l2_flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    return sum(ts) / len(ts)
+
+
+def measure_extras(nea, w, q, k, v, do, o, lse, wsp, l2_flush, stream, peak_hbm, src, reps):
+    """The rows beyond the training step: RoPE (rotation pass and the cost of
+    the inverse rotation fused into the backward) on this workload, and
+    decode attention on the decode workloads.  Each is timed alone with CUDA
+    events, L2 flushed before every call."""
+    import torch
+    from causal_gqa_flashattention_gb300.workloads import DECODE_WORKLOADS, make_decode_inputs
+    out = {}
+    cs = nea.rope_table(w.N, w.d, device=q.device)
+    qr, kr = torch.empty_like(q), torch.empty_like(k)
+    t_rot = _time_ms(lambda: nea.rope_qk(q, k, cs, qr=qr, kr=kr, stream=stream), l2_flush,
+                     stream, reps)
+    rot_bytes = 2 * (q.numel() + k.numel()) * q.element_size() + cs.numel() * 4
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    t_b = _time_ms(lambda: nea.attn_bwd(qr, kr, v, o, do, lse, dq=dq, dk=dk, dv=dv,
+                                        workspace=wsp, stream=stream), l2_flush, stream, reps)
+    t_br = _time_ms(lambda: nea.attn_bwd(qr, kr, v, o, do, lse, dq=dq, dk=dk, dv=dv,
+                                         workspace=wsp, stream=stream, rope_cs=cs),
+                    l2_flush, stream, reps)
+    out["rope_qk"] = {"ms": round(t_rot, 5), "bytes": rot_bytes,
+                      "gbs": round(rot_bytes / (t_rot * 1e-3) / 1e9, 1),
+                      "hbm_frac": round(rot_bytes / (t_rot * 1e-3) / 1e9 / peak_hbm, 3),
+                      "peak_source": f"hbm_gbs of {src}"}
+    out["bwd_rope"] = {"ms": round(t_br, 5), "ms_without_rope": round(t_b, 5),
+                       "overhead_pct": round(100.0 * (t_br / t_b - 1.0), 2)}
+    for name, dw in DECODE_WORKLOADS.items():
+        dq_, kc, vc, lens = make_decode_inputs(dw, seed=0, device=q.device)
+        od = torch.empty_like(dq_)
+        ld = torch.empty((dw.B, dw.H, dw.nq), dtype=torch.float32, device=q.device)
+        wsd = torch.empty(max(nea.decode_workspace_bytes(dw.B, dw.H, dw.Hkv, dw.nq, dw.Lmax,
+                                                          dw.d), 1),
+                          dtype=torch.uint8, device=q.device)
+        t = _time_ms(lambda: nea.attn_decode(dq_, kc, vc, lens, out=od, lse=ld, workspace=wsd,
+                                             stream=stream), l2_flush, stream, reps)
+        byt = dw.cache_bytes() + 2 * dq_.numel() * dq_.element_size() + ld.numel() * 4
+        out[name] = {"ms": round(t, 5), "bytes": byt,
+                     "gbs": round(byt / (t * 1e-3) / 1e9, 1),
+                     "hbm_frac": round(byt / (t * 1e-3) / 1e9 / peak_hbm, 3),
+                     "config": {"B": dw.B, "H": dw.H, "Hkv": dw.Hkv, "nq": dw.nq,
+                                "Lmax": dw.Lmax, "d": dw.d, "dtype": dw.dtype},
+                     "peak_source": f"hbm_gbs of {src}", "launches": 2}
+    return out
 
 
 def oracle_sample(w, nb):
@@ -427,6 +492,8 @@ def main():
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the RoPE and decode measurements")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(
         ["tiny_f32", "gpt2s_bf16", "gpt2s_f32", "long_bf16", "wide_bf16"]),
         help="default: the GPT-2-small bf16 shape, the headline measurement")

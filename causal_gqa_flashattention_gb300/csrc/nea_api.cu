@@ -347,6 +347,53 @@ int nea_attn_bwd_rope(const void* Qr, const void* Kr, const void* V, const void*
   return NEA_OK;
 }
 
+static int decode_checks(int B, int H, int Hkv, int nq, int Lmax, int d, int dtype) {
+  if (B < 1 || H < 1 || Hkv < 1 || nq < 1 || Lmax < nq || H % Hkv != 0) return NEA_ERR_INVALID;
+  if (dtype != NEA_BF16 && dtype != NEA_F32) return NEA_ERR_INVALID;
+  if (d != 64 && d != 128) return NEA_ERR_UNSUPPORTED;
+  if ((H / Hkv) * nq > kMaxDecodeRows) return NEA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Hkv > 65535 || Lmax > (1 << 24) ||
+      static_cast<long long>(B) * H * nq > (1LL << 30))
+    return NEA_ERR_UNSUPPORTED;
+  return NEA_OK;
+}
+
+size_t nea_attn_decode_workspace_bytes(int B, int H, int Hkv, int nq, int Lmax, int d) {
+  if (decode_checks(B, H, Hkv, nq, Lmax, d, NEA_BF16) != NEA_OK) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * nq;
+  const size_t nchunk = (static_cast<size_t>(Lmax) + decode_chunk_rows() - 1) / decode_chunk_rows();
+  return align256(rows * nchunk * d * sizeof(float)) + align256(rows * nchunk * sizeof(float2));
+}
+
+int nea_attn_decode(const void* Q, const void* Kc, const void* Vc, const int* lens, void* O,
+                    float* LSE, void* workspace, size_t workspace_bytes, int B, int H, int Hkv,
+                    int nq, int Lmax, int d, float scale, int dtype, void* stream) {
+  if (!aligned16(Q) || !aligned16(Kc) || !aligned16(Vc) || !aligned16(O) || !aligned16(LSE) ||
+      !lens || (reinterpret_cast<uintptr_t>(lens) & 3u) != 0)
+    return NEA_ERR_INVALID;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return NEA_ERR_INVALID;
+  int st = decode_checks(B, H, Hkv, nq, Lmax, d, dtype);
+  if (st != NEA_OK) return st;
+  const size_t need = nea_attn_decode_workspace_bytes(B, H, Hkv, nq, Lmax, d);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < need)
+    return NEA_ERR_WORKSPACE;
+  DecodeArgs a;
+  std::memset(&a, 0, sizeof(a));
+  const size_t rows = static_cast<size_t>(B) * H * nq;
+  a.nchunk = (Lmax + decode_chunk_rows() - 1) / decode_chunk_rows();
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.opart = reinterpret_cast<float*>(ws);
+  a.ml = reinterpret_cast<float2*>(ws + align256(rows * a.nchunk * d * sizeof(float)));
+  a.Q = Q; a.Kc = Kc; a.Vc = Vc; a.lens = lens; a.O = O; a.lse = LSE;
+  a.status = status_ptr();
+  if (!a.status) return NEA_ERR_CUDA;
+  a.B = B; a.H = H; a.Hkv = Hkv; a.nq = nq; a.Lmax = Lmax; a.d = d; a.dtype = dtype;
+  a.scale = scale;
+  return launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? NEA_OK
+                                                                           : NEA_ERR_CUDA;
+}
+
 int nea_attn_check_status(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return NEA_ERR_CUDA;
@@ -354,6 +401,7 @@ int nea_attn_check_status(void* stream) {
   if (cudaMemcpyFromSymbol(&word, g_status_word, sizeof(word)) != cudaSuccess) return NEA_ERR_CUDA;
   if (word != 0 && cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess)
     return NEA_ERR_CUDA;
+  if (word & kStatusBadLength) return NEA_ERR_INVALID;
   return word != 0 ? NEA_ERR_TIMEOUT : NEA_OK;
 }
 

@@ -45,6 +45,24 @@ struct BwdArgs {
   int dtype;
 };
 
+// Decode attention over a key/value cache (split over the cache length).
+constexpr int kMaxDecodeRows = 32;  // G * nq query rows per KV head at most
+constexpr unsigned int kStatusBadLength = 2u;  // a cache length outside [nq, Lmax]
+struct DecodeArgs {
+  const void* Q;       // [B][H][nq][d] dtype
+  const void* Kc;      // [B][Hkv][Lmax][d] dtype
+  const void* Vc;
+  const int* lens;     // [B] valid cache rows per batch element (device)
+  void* O;             // [B][H][nq][d] dtype
+  float* lse;          // [B][H][nq]
+  float* opart;        // workspace: [B*H*nq][nchunk][d] partial P V
+  float2* ml;          // workspace: [B*H*nq][nchunk] (max, sum) per chunk
+  unsigned int* status;
+  int B, H, Hkv, nq, Lmax, d, nchunk, dtype;
+  float scale;
+};
+int decode_chunk_rows();
+
 // Each launcher validates nothing (the API layer did) and returns the
 // cudaError_t of its launch(es).
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
@@ -58,6 +76,7 @@ cudaError_t launch_bwd_main_f32(const BwdArgs& a, const CUtensorMap& tmQt,
                                 const CUtensorMap& tmdOt, const CUtensorMap& tmKt,
                                 cudaStream_t stream);
 // Rotary embedding: the (cos, sin) table [N][d/2], and Qr = R(Q), Kr = R(K).
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_rope_table(float2* cs, int N, int d, double base, cudaStream_t stream);
 cudaError_t launch_rope_rotate(const void* Q, const void* K, void* Qr, void* Kr,
                                const float2* cs, long long qrows, long long krows, int N, int d,

@@ -70,6 +70,10 @@ def lib():
             L.nea_attn_bwd_rope.argtypes = [_vp] * 11 + [ctypes.c_size_t] + [_i] * 5 + [
                 _f, _i, _i, _vp]
             L.nea_attn_bwd_rope.restype = _i
+            L.nea_attn_decode_workspace_bytes.argtypes = [_i] * 6
+            L.nea_attn_decode_workspace_bytes.restype = ctypes.c_size_t
+            L.nea_attn_decode.argtypes = [_vp] * 7 + [ctypes.c_size_t] + [_i] * 6 + [_f, _i, _vp]
+            L.nea_attn_decode.restype = _i
             L.nea_attn_check_status.argtypes = [_vp]
             L.nea_attn_check_status.restype = _i
             L.nea_status_string.argtypes = [_i]
@@ -219,6 +223,39 @@ def attn_bwd_stages(q, k, v, o, do, lse, dq, dk, dv, workspace, *, causal=True, 
     if between:
         between(3)
     return dq, dk, dv
+
+
+def decode_workspace_bytes(B, H, Hkv, nq, Lmax, d) -> int:
+    return int(lib().nea_attn_decode_workspace_bytes(B, H, Hkv, nq, Lmax, d))
+
+
+def attn_decode(q, k_cache, v_cache, lens, *, scale=None, out=None, lse=None, workspace=None,
+                stream=None):
+    """Decode attention of q [B,H,nq,d] (the newest nq tokens) against caches
+    [B,Hkv,Lmax,d] with ``lens`` [B] int32 (device) valid rows each, the new
+    tokens included.  Returns (O [B,H,nq,d], LSE [B,H,nq])."""
+    for t in (q, k_cache, v_cache, lens):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA tensors")
+    if lens.dtype != torch.int32:
+        raise TypeError("lens must be int32")
+    B, H, nq, d = q.shape
+    Hkv, Lmax = k_cache.shape[1], k_cache.shape[2]
+    if k_cache.shape != (B, Hkv, Lmax, d) or v_cache.shape != k_cache.shape:
+        raise ValueError("caches must be [B, Hkv, Lmax, d]")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    lse_t = torch.empty((B, H, nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    need = decode_workspace_bytes(B, H, Hkv, nq, Lmax, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = lib().nea_attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(lens), _ptr(o),
+                               _ptr(lse_t), _ptr(workspace), workspace.numel(), B, H, Hkv, nq,
+                               Lmax, d, scale, _dtype_code(q),
+                               ctypes.c_void_p(_stream_handle(stream)))
+    if st != NEA_OK:
+        raise NeaError(st, "nea_attn_decode")
+    return o, lse_t
 
 
 def check_status(stream=None) -> int:

@@ -101,3 +101,61 @@ def make_inputs(w: Workload, seed: int = 0, device=None):
 def custom(B, H, Hkv, N, d, dtype="bf16", causal=True, qk_std=1.0, vdo="normal") -> Workload:
     return Workload(f"B{B}_H{H}_Hkv{Hkv}_N{N}_d{d}_{dtype}{'' if causal else '_full'}",
                     B, H, Hkv, N, d, dtype, qk_std, vdo, causal)
+
+
+@dataclass(frozen=True)
+class DecodeWorkload:
+    """One decode step: the newest nq tokens of B sequences against a cache of
+    Lmax rows per sequence, lens[b] of them valid (new tokens included)."""
+    name: str
+    B: int
+    H: int
+    Hkv: int
+    nq: int
+    Lmax: int
+    d: int
+    dtype: str
+    lens: tuple = ()     # empty: every sequence fills the cache (lens[b] = Lmax)
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+    @property
+    def esize(self) -> int:
+        return 2 if self.dtype == "bf16" else 4
+
+    def lengths(self):
+        return list(self.lens) if self.lens else [self.Lmax] * self.B
+
+    def cache_bytes(self) -> int:
+        """K and V rows the step must read (the valid ones), in bytes."""
+        return 2 * self.Hkv * sum(self.lengths()) * self.d * self.esize
+
+
+DECODE_WORKLOADS = {
+    # one generated token per sequence at the training shape's full context
+    "decode_gpt2s_bf16": DecodeWorkload("decode_gpt2s_bf16", 8, 12, 4, 1, 1024, 64, "bf16"),
+    # a long cache, large enough to be bound by HBM bandwidth
+    "decode_long_bf16": DecodeWorkload("decode_long_bf16", 32, 12, 4, 1, 16384, 64, "bf16"),
+}
+
+
+def make_decode_inputs(w: DecodeWorkload, seed: int = 0, device=None):
+    """Return (q, k_cache, v_cache, lens): q [B,H,nq,d], caches [B,Hkv,Lmax,d]
+    drawn N(0,1) in that order from a CPU generator seeded with ``seed``, then
+    rounded to the dtype; lens [B] int32."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    q = torch.randn((w.B, w.H, w.nq, w.d), generator=g, dtype=torch.float32)
+    kc = torch.randn((w.B, w.Hkv, w.Lmax, w.d), generator=g, dtype=torch.float32)
+    vc = torch.randn((w.B, w.Hkv, w.Lmax, w.d), generator=g, dtype=torch.float32)
+    lens = torch.tensor(w.lengths(), dtype=torch.int32)
+    out = [t.to(w.torch_dtype).contiguous() for t in (q, kc, vc)] + [lens]
+    if device is not None:
+        out = [t.to(device) for t in out]
+    return tuple(out)

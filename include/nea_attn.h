@@ -205,9 +205,33 @@ int nea_attn_bwd_rope(const void* Qr, const void* Kr, const void* V, const void*
                       int N, int d, float scale, int causal, int dtype, void* stream);
 
 /*
+ * Decode attention: the nq newest tokens of each sequence against its
+ * key/value cache (the inference use the pages mention: "NanoEuler:
+ * Hand-writing GPT-2 in Pure C/CUDA", FAQ on production inference).
+ * Reading taken: batch element b's cache holds lens[b] valid rows, the new
+ * tokens' own keys and values included, so new token t sits at position
+ * lens[b] - nq + t and sees cache rows 0 .. lens[b] - nq + t.
+ *   Q, O    [B][H][nq][d] dtype       Kc, Vc  [B][Hkv][Lmax][d] dtype
+ *   LSE     [B][H][nq] fp32, natural log of the scaled logits
+ *   lens    [B] int32, DEVICE memory, nq <= lens[b] <= Lmax; a length out
+ *           of that range is clamped into it and reported by
+ *           nea_attn_check_status() as NEA_ERR_INVALID.
+ * Supported: d in {64, 128}; bf16 or fp32; (H / Hkv) * nq <= 32.
+ * The cache is read once per KV head, split over the cache length in
+ * 128-row chunks (one CTA per chunk and KV head) and combined by a second
+ * kernel through `workspace` (nea_attn_decode_workspace_bytes() bytes,
+ * 256-byte aligned, caller-owned, contents on entry irrelevant).
+ */
+size_t nea_attn_decode_workspace_bytes(int B, int H, int Hkv, int nq, int Lmax, int d);
+int nea_attn_decode(const void* Q, const void* Kc, const void* Vc, const int* lens, void* O,
+                    float* LSE, void* workspace, size_t workspace_bytes, int B, int H, int Hkv,
+                    int nq, int Lmax, int d, float scale, int dtype, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the library's device status
- * word.  Returns NEA_ERR_TIMEOUT if a kernel's bounded wait gave up since
- * the last check, NEA_ERR_CUDA if the stream reports an error, else NEA_OK.
+ * word.  Returns NEA_ERR_INVALID if a decode call met a cache length outside
+ * [nq, Lmax], NEA_ERR_TIMEOUT if a kernel's bounded wait gave up since the
+ * last check, NEA_ERR_CUDA if the stream reports an error, else NEA_OK.
  */
 int nea_attn_check_status(void* stream);
 

@@ -29,7 +29,8 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("nea_attn_fwd", "nea_attn_bwd", "nea_attn_bwd_workspace_bytes",
               "nea_attn_check_status", "nea_status_string", "nea_version",
-              "nea_rope_table", "nea_rope_qk", "nea_attn_bwd_rope"):
+              "nea_rope_table", "nea_rope_qk", "nea_attn_bwd_rope", "nea_attn_decode",
+              "nea_attn_decode_workspace_bytes"):
         assert n in names
 
 
@@ -132,3 +133,28 @@ def test_rope_argument_checks(nea):
     assert L.nea_rope_qk(*args([P] * 5, d=96)) == -2                       # unsupported d
     bw = [vp(P)] * 6 + [vp(0)] + [vp(P)] * 4
     assert L.nea_attn_bwd_rope(*bw, 1 << 40, 2, 12, 4, 1024, 64, 0.125, 1, 0, None) == -1
+
+
+def test_decode_argument_checks(nea):
+    L = nea.lib()
+    vp = ctypes.c_void_p
+
+    def dec(ptrs=None, ws=P, wsb=1 << 40, B=2, H=12, Hkv=4, nq=1, Lmax=1024, d=64, scale=0.125,
+            dtype=0):
+        ptrs = ptrs or [P] * 6
+        return L.nea_attn_decode(*[vp(x) for x in ptrs], vp(ws), wsb, B, H, Hkv, nq, Lmax, d,
+                                 scale, dtype, None)
+    assert dec(ptrs=[P, P, P, 0, P, P]) == -1            # null lens
+    assert dec(ptrs=[P, P, P, P + 2, P, P]) == -1        # misaligned lens
+    assert dec(ptrs=[P + 8, P, P, P, P, P]) == -1        # misaligned Q
+    assert dec(H=12, Hkv=5) == -1
+    assert dec(nq=0) == -1
+    assert dec(nq=8, Lmax=4) == -1                        # cache shorter than the new tokens
+    assert dec(scale=0.0) == -1
+    assert dec(d=96) == -2
+    assert dec(nq=11) == -2                               # 3 * 11 query rows > 32
+    assert dec(ws=0) == -5
+    assert dec(wsb=16) == -5
+    need = nea.decode_workspace_bytes(2, 12, 4, 1, 1024, 64)
+    assert need >= 2 * 12 * 8 * 64 * 4 + 2 * 12 * 8 * 8
+    assert nea.decode_workspace_bytes(2, 12, 4, 11, 1024, 64) == 0

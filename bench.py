@@ -399,6 +399,13 @@ def measure_extras(nea, w, q, k, v, do, o, lse, wsp, l2_flush, stream, peak_hbm,
     t_br = _time_ms(lambda: nea.attn_bwd(qr, kr, v, o, do, lse, dq=dq, dk=dk, dv=dv,
                                          workspace=wsp, stream=stream, rope_cs=cs),
                     l2_flush, stream, reps)
+    t_det = _time_ms(lambda: nea.attn_bwd(qr, kr, v, o, do, lse, dq=dq, dk=dk, dv=dv,
+                                          workspace=wsp, stream=stream, deterministic=True),
+                     l2_flush, stream, reps)
+    out["bwd_deterministic"] = {"ms": round(t_det, 5), "ms_default": round(t_b, 5),
+                                "tflops": round(w.bwd_flops() / (t_det * 1e-3) / 1e12, 1),
+                                "note": "dQ by one CTA per query tile (S and dP recomputed); "
+                                        "tflops counts the default path's 5 GEMMs"}
     out["rope_qk"] = {"ms": round(t_rot, 5), "bytes": rot_bytes,
                       "gbs": round(rot_bytes / (t_rot * 1e-3) / 1e9, 1),
                       "hbm_frac": round(rot_bytes / (t_rot * 1e-3) / 1e9 / peak_hbm, 3),

@@ -196,7 +196,9 @@ enum : int {
   C_DRAIN, C_DRAIN2, C_QFULL  // then QFULL[QST], DOFULL[QST], QEMPTY[QST]
 };
 
-template <int D>
+// DQ = false: dK and dV only (the deterministic backward computes dQ in a
+// kernel of its own, one CTA per query tile); no dQ MMA and no reductions.
+template <int D, bool DQ>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const __grid_constant__ BwdArgs a) {
   using C = BwdCfg<D>;
   constexpr int QST = C::QST;
@@ -378,7 +380,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
         // dP_{n+1}: the compute warps have read dP_n (DSFULL_n); with d = 128
         // dQ_n shares dP's columns and must have been drained (DQFREE_n)
         if (!wait_do(n + 1, 24) || !mbar_wait(bar(C_DSFULL), n & 1, abort, 25, status)) break;
-        if (C::DQ_ALIAS_DP && !mbar_wait(bar(C_DQFREE), n & 1, abort, 25, status)) break;
+        if (DQ && C::DQ_ALIAS_DP && !mbar_wait(bar(C_DQFREE), n & 1, abort, 25, status)) break;
         tc_fence_after();
         issue_dp(n + 1);
       }
@@ -408,18 +410,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
                                  (n > 0 || k > 0) ? 1u : 0u);
         }
         mma_commit(qempty(s));  // Q_i no longer read by B
-        // dQ_i = dS K_j (the dQ warps have drained dQ_{n-1} when d = 64)
-        if (!C::DQ_ALIAS_DP && n > 0 && !mbar_wait(bar(C_DQFREE), (n - 1) & 1, abort, 28, status))
-          break;
-        tc_fence_after();
+        if (DQ) {
+          // dQ_i = dS K_j (the dQ warps have drained dQ_{n-1} when d = 64)
+          if (!C::DQ_ALIAS_DP && n > 0 &&
+              !mbar_wait(bar(C_DQFREE), (n - 1) & 1, abort, 28, status))
+            break;
+          tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < C::NK_T; ++k)
-          mma_ss<MmaKind::kBF16>(tmem + C::DQ_COL,
-                                 sdesc_sw128(sDS + k * 16 * 128, C::BLK_BYTES, 1024),
-                                 sdesc_sw128(sK + k * 16 * 128, C::BLK_BYTES, 1024), idDQ,
-                                 k > 0 ? 1u : 0u);
+          for (int k = 0; k < C::NK_T; ++k)
+            mma_ss<MmaKind::kBF16>(tmem + C::DQ_COL,
+                                   sdesc_sw128(sDS + k * 16 * 128, C::BLK_BYTES, 1024),
+                                   sdesc_sw128(sK + k * 16 * 128, C::BLK_BYTES, 1024), idDQ,
+                                   k > 0 ? 1u : 0u);
+        }
         mma_commit(bar(C_DSEMPTY));
-        mma_commit(bar(C_DQFULL));
+        if (DQ) mma_commit(bar(C_DQFULL));
       }
       mma_commit(bar(C_FINAL));
       mma_commit(bar(C_DRAIN2));
@@ -561,7 +566,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
         }
       }
     }
-  } else if (warp >= 12) {
+  } else if (DQ && warp >= 12) {
     // ------------------------------------------------------------ dQ
     const int quad = warp & 3;
     const int qr = quad * 32 + lane;  // query row == TMEM lane of the dQ tile
@@ -619,10 +624,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
 }
 
 
-template <int D>
+template <int D, bool DQ>
 cudaError_t launch_main_t(const BwdArgs& a, cudaStream_t stream) {
   using C = BwdCfg<D>;
-  auto kern = bwd_main_kernel<D>;
+  auto kern = bwd_main_kernel<D, DQ>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -658,8 +663,11 @@ cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
-  if (a.dtype == 0 && a.d == 64) return launch_main_t<64>(a, stream);
-  if (a.dtype == 0 && a.d == 128) return launch_main_t<128>(a, stream);
+  if (a.dtype == 0 && a.d == 64)
+    return a.deterministic ? launch_main_t<64, false>(a, stream) : launch_main_t<64, true>(a, stream);
+  if (a.dtype == 0 && a.d == 128)
+    return a.deterministic ? launch_main_t<128, false>(a, stream)
+                           : launch_main_t<128, true>(a, stream);
   return cudaErrorInvalidValue;
 }
 

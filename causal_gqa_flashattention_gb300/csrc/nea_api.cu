@@ -329,22 +329,43 @@ int nea_rope_qk(const void* Q, const void* K, void* Qr, void* Kr, const float* c
              : NEA_ERR_CUDA;
 }
 
-int nea_attn_bwd_rope(const void* Qr, const void* Kr, const void* V, const void* O,
-                      const void* dO, const float* LSE, const float* cos_sin, void* dQ, void* dK,
-                      void* dV, void* workspace, size_t workspace_bytes, int B, int H, int Hkv,
-                      int N, int d, float scale, int causal, int dtype, void* stream) {
-  if (!aligned16(cos_sin)) return NEA_ERR_INVALID;
+int nea_attn_bwd_ex(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                    const float* LSE, const float* rope_cos_sin, int flags, void* dQ, void* dK,
+                    void* dV, void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int N,
+                    int d, float scale, int causal, int dtype, void* stream) {
+  if ((flags & ~NEA_BWD_DETERMINISTIC) != 0) return NEA_ERR_INVALID;
+  if (rope_cos_sin != nullptr && !aligned16(rope_cos_sin)) return NEA_ERR_INVALID;
   BwdArgs a;
-  int st = prepare_bwd(&a, Qr, Kr, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes, B, H,
+  int st = prepare_bwd(&a, Q, K, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes, B, H,
                        Hkv, N, d, scale, causal, dtype, true, true, true);
   if (st != NEA_OK) return st;
-  a.rope_cs = reinterpret_cast<const float2*>(cos_sin);
+  a.rope_cs = reinterpret_cast<const float2*>(rope_cos_sin);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == NEA_BF16 && (flags & NEA_BWD_DETERMINISTIC)) {
+    // dK, dV from the main kernel without its dQ part; dQ from one CTA per
+    // query tile; no accumulator to clear or cast
+    a.deterministic = 1;
+    a.dq_acc = nullptr;
+    if (launch_bwd_pre(a, s) != cudaSuccess || launch_bwd_main(a, s) != cudaSuccess ||
+        launch_bwd_dq(a, s) != cudaSuccess)
+      return NEA_ERR_CUDA;
+    return NEA_OK;
+  }
+  // fp32 already owns each dQ tile in one CTA, so it is deterministic as is
   if (launch_bwd_pre(a, s) != cudaSuccess) return NEA_ERR_CUDA;
   st = run_main(a, s);
   if (st != NEA_OK) return st;
   if (dtype == NEA_BF16 && launch_bwd_post(a, s) != cudaSuccess) return NEA_ERR_CUDA;
   return NEA_OK;
+}
+
+int nea_attn_bwd_rope(const void* Qr, const void* Kr, const void* V, const void* O,
+                      const void* dO, const float* LSE, const float* cos_sin, void* dQ, void* dK,
+                      void* dV, void* workspace, size_t workspace_bytes, int B, int H, int Hkv,
+                      int N, int d, float scale, int causal, int dtype, void* stream) {
+  if (!aligned16(cos_sin)) return NEA_ERR_INVALID;
+  return nea_attn_bwd_ex(Qr, Kr, V, O, dO, LSE, cos_sin, 0, dQ, dK, dV, workspace,
+                         workspace_bytes, B, H, Hkv, N, d, scale, causal, dtype, stream);
 }
 
 static int decode_checks(int B, int H, int Hkv, int nq, int Lmax, int d, int dtype) {

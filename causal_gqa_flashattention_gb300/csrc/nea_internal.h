@@ -39,6 +39,7 @@ struct BwdArgs {
   void* dV;
   const float2* rope_cs;            // null, or RoPE (cos, sin) [N][d/2]: dQ, dK are mapped
                                     // back through the inverse rotation before they are stored
+  int deterministic;                // bf16: dQ by one CTA per query tile (no reductions)
   unsigned int* status;
   int B, H, Hkv, N, d, causal;
   float scale;
@@ -69,6 +70,8 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_post(const BwdArgs& a, cudaStream_t stream);
+// Deterministic bf16 dQ: one CTA per query tile walks its key tiles in order.
+cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream);
 // fp32 path: transposes for the workspace, then the dK/dV and dQ kernels.
 cudaError_t launch_transpose_f32(const float* src, float* dst, long long heads, int N,
                                  cudaStream_t stream);

@@ -70,6 +70,9 @@ def lib():
             L.nea_attn_bwd_rope.argtypes = [_vp] * 11 + [ctypes.c_size_t] + [_i] * 5 + [
                 _f, _i, _i, _vp]
             L.nea_attn_bwd_rope.restype = _i
+            L.nea_attn_bwd_ex.argtypes = [_vp] * 7 + [_i] + [_vp] * 4 + [ctypes.c_size_t] + [
+                _i] * 5 + [_f, _i, _i, _vp]
+            L.nea_attn_bwd_ex.restype = _i
             L.nea_attn_decode_workspace_bytes.argtypes = [_i] * 6
             L.nea_attn_decode_workspace_bytes.restype = ctypes.c_size_t
             L.nea_attn_decode.argtypes = [_vp] * 7 + [ctypes.c_size_t] + [_i] * 6 + [_f, _i, _vp]
@@ -157,13 +160,16 @@ def rope_qk(q, k, cos_sin, *, qr=None, kr=None, stream=None):
     return qr, kr
 
 
+NEA_BWD_DETERMINISTIC = 1
+
+
 def attn_bwd(q, k, v, o, do, lse, *, causal=True, scale=None, dq=None, dk=None, dv=None,
-             workspace=None, stream=None, rope_cs=None):
+             workspace=None, stream=None, rope_cs=None, deterministic=False):
     """dQ, dK, dV for upstream gradient ``do``, using the forward's O and LSE.
 
     With ``rope_cs`` (the table ``q`` and ``k`` were rotated with), ``q`` and
     ``k`` are the rotated inputs and dQ, dK are returned with respect to the
-    unrotated ones."""
+    unrotated ones.  ``deterministic`` selects the bit-reproducible dQ path."""
     B, H, Hkv, N, d = _check(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     code = _dtype_code(q)
@@ -173,7 +179,14 @@ def attn_bwd(q, k, v, o, do, lse, *, causal=True, scale=None, dq=None, dk=None, 
     need = bwd_workspace_bytes(B, H, Hkv, N, d, code)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-    if rope_cs is None:
+    if deterministic:
+        st = lib().nea_attn_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
+                                   _ptr(rope_cs), NEA_BWD_DETERMINISTIC, _ptr(dq), _ptr(dk),
+                                   _ptr(dv), _ptr(workspace), workspace.numel(), B, H, Hkv, N, d,
+                                   scale, int(bool(causal)), code,
+                                   ctypes.c_void_p(_stream_handle(stream)))
+        what = "nea_attn_bwd_ex"
+    elif rope_cs is None:
         st = lib().nea_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
                                 _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(), B, H,
                                 Hkv, N, d, scale, int(bool(causal)), code,

@@ -96,7 +96,8 @@ size_t nea_attn_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d, int dty
  * nea_attn_bwd_workspace_bytes(...) bytes, 256-byte aligned, owned by the
  * caller and not used concurrently by another call; its contents on entry
  * do not matter.  The order of the dQ additions is not fixed, so dQ may
- * differ between runs in the last bits; dK and dV are deterministic.
+ * differ between runs in the last bits; dK and dV are deterministic (for a
+ * bit-reproducible dQ see nea_attn_bwd_ex() with NEA_BWD_DETERMINISTIC).
  */
 int nea_attn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
                  const float* LSE, void* dQ, void* dK, void* dV, void* workspace,
@@ -203,6 +204,26 @@ int nea_attn_bwd_rope(const void* Qr, const void* Kr, const void* V, const void*
                       const void* dO, const float* LSE, const float* cos_sin, void* dQ, void* dK,
                       void* dV, void* workspace, size_t workspace_bytes, int B, int H, int Hkv,
                       int N, int d, float scale, int causal, int dtype, void* stream);
+
+/*
+ * Backward with options.  Arguments as nea_attn_bwd(), plus:
+ *   rope_cos_sin  null, or the RoPE table Q and K were rotated with (then Q
+ *                 and K are the rotated inputs and dQ, dK come back with
+ *                 respect to the unrotated ones, as nea_attn_bwd_rope());
+ *   flags         0, or NEA_BWD_DETERMINISTIC: bit-reproducible gradients.
+ *                 bf16: the main kernel computes dK and dV only and a second
+ *                 kernel computes dQ with one CTA per 128-row query tile,
+ *                 walking the key tiles in a fixed order (S and dP are
+ *                 recomputed there: two more GEMMs per tile pair, no dQ
+ *                 accumulator traffic).  fp32 is deterministic either way.
+ *                 Other bits: NEA_ERR_INVALID.
+ * The workspace is the one nea_attn_bwd_workspace_bytes() sizes.
+ */
+#define NEA_BWD_DETERMINISTIC 1
+int nea_attn_bwd_ex(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                    const float* LSE, const float* rope_cos_sin, int flags, void* dQ, void* dK,
+                    void* dV, void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int N,
+                    int d, float scale, int causal, int dtype, void* stream);
 
 /*
  * Decode attention: the nq newest tokens of each sequence against its

@@ -29,7 +29,8 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("nea_attn_fwd", "nea_attn_bwd", "nea_attn_bwd_workspace_bytes",
               "nea_attn_check_status", "nea_status_string", "nea_version",
-              "nea_rope_table", "nea_rope_qk", "nea_attn_bwd_rope", "nea_attn_decode",
+              "nea_rope_table", "nea_rope_qk", "nea_attn_bwd_rope", "nea_attn_bwd_ex",
+              "nea_attn_decode",
               "nea_attn_decode_workspace_bytes"):
         assert n in names
 
@@ -158,3 +159,19 @@ def test_decode_argument_checks(nea):
     need = nea.decode_workspace_bytes(2, 12, 4, 1, 1024, 64)
     assert need >= 2 * 12 * 8 * 64 * 4 + 2 * 12 * 8 * 8
     assert nea.decode_workspace_bytes(2, 12, 4, 11, 1024, 64) == 0
+
+
+def test_bwd_ex_argument_checks(nea):
+    L = nea.lib()
+    vp = ctypes.c_void_p
+    ptrs = [vp(P)] * 6
+
+    def ex(flags, cs=P, ws=P):
+        return L.nea_attn_bwd_ex(*ptrs, vp(cs), flags, vp(P), vp(P), vp(P), vp(ws), 1 << 40,
+                                 2, 12, 4, 1024, 64, 0.125, 1, 0, None)
+    assert ex(2) == -1               # unknown flag bit
+    assert ex(-1) == -1
+    assert ex(1, cs=P + 4) == -1     # misaligned RoPE table
+    assert ex(1, ws=0) == -5         # no workspace
+    assert L.nea_attn_bwd_ex(*ptrs, vp(0), 1, vp(P), vp(P), vp(P), vp(P), 1 << 40, 2, 12, 5,
+                             1024, 64, 0.125, 1, 0, None) == -1   # bad group

@@ -237,7 +237,7 @@ def run_cuda(args):
 
     def l2_flush():
         flush.zero_()
-        flush.view(torch.int32).sum()  # the read-back leaves L2 holding clean lines
+        flush.view(torch.float32).sum()  # read-back (no copy): L2 left holding clean lines
 
     def step(evs=None):
         if evs:

@@ -16,9 +16,12 @@
 //                  P V (thread = output column) into the workspace;
 //  decode_combine  per query row, rescales the chunks' partials to the
 //                  common max and normalises: O (dtype) and LSE (natural log).
+#include <algorithm>
+
 #include <cuda_bf16.h>
 
 #include "nea_internal.h"
+#include "ptx.cuh"
 
 namespace nea {
 namespace {
@@ -82,138 +85,256 @@ __device__ __forceinline__ int cache_len(const DecodeArgs& a, int b) {
 
 // RM: the query-row bound the loops are unrolled for (the smallest of 4, 8,
 // 16, 32 that holds G * nq), so that no work is spent on absent rows.
-// Shared memory is read through broadcasts and 16-byte vectors: the kernel
-// would otherwise be bound by shared-memory instructions, not by HBM.
-template <typename T, int D, int RM>
-__global__ void __launch_bounds__(kChunk) decode_partial_kernel(const DecodeArgs a) {
-  extern __shared__ float sm[];
-  float* q_s = sm;                      // [RM][D], scaled to log2 units
-  float* p_s = q_s + RM * D;            // [RM][kChunk] P of the chunk
-  float* red = p_s + RM * kChunk;       // [2][4 warps][RM] partial max / sum
-  T* v_s = reinterpret_cast<T*>(red + 2 * 4 * RM);  // [kChunk][D], the cache's dtype
+//
+// One CTA per (split, batch, KV head) streams `cps` consecutive 128-row
+// chunks of the cache through a ring of STAGES shared-memory stages filled
+// by TMA (K and V tiles, 128-byte swizzle: a thread reading its own key row
+// and a warp reading one V row both touch distinct banks), so the next
+// chunk's loads are in flight while this one is computed.  Per chunk:
+// scores (thread = cache row), the chunk's row max and P, then P V (warp w
+// owns rows w, w + 4, ...; lane l owns CPL adjacent columns) folded into a
+// running (max, sum, O) per row -- the online softmax across the split.
+template <typename T, int D, int RM, int STAGES>
+__global__ void __launch_bounds__(kChunk) decode_partial_kernel(const __grid_constant__ DecodeArgs a) {
+  constexpr int ES = static_cast<int>(sizeof(T));
+  constexpr int TILE = kChunk * D * ES;     // one K or V tile
+  constexpr int NBLK = D * ES / 128;        // 128-byte column blocks per row
+  constexpr int BLK = kChunk * 128;         // bytes per block
+  constexpr int EV = 16 / ES;               // elements per 16-byte chunk
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  __shared__ __align__(8) uint64_t full[STAGES];
+  __shared__ int abort_sh;
+  float* q_s = reinterpret_cast<float*>(smem + 2 * STAGES * TILE);  // [RM][D], log2 units
+  float* p_s = q_s + RM * D;                                        // [RM][kChunk]
+  float* red = p_s + RM * kChunk;                                   // [2][4][RM]
+  float* red_o = red + 8 * RM;  // RM == 4: [4 warps][4 rows][D] partial P V
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int c = blockIdx.x, bg = blockIdx.y;
+  const int split = blockIdx.x, bg = blockIdx.y;
   const int b = bg / a.Hkv, g = bg % a.Hkv, G = a.H / a.Hkv, R = G * a.nq;
   const int L = cache_len(a, b);
-  const int c0 = c * kChunk;
-  if (c0 >= L) return;  // past this element's cache: the combine skips the chunk
-  const T* Q = static_cast<const T*>(a.Q);
-  const T* K = static_cast<const T*>(a.Kc) + (static_cast<size_t>(b) * a.Hkv + g) * a.Lmax * D;
-  const T* V = static_cast<const T*>(a.Vc) + (static_cast<size_t>(b) * a.Hkv + g) * a.Lmax * D;
-  const float cq = a.scale * kLog2e;
-  // this thread's cache row: its keys are loaded first, as 16-byte vectors,
-  // so that they are in flight together with the V chunk's loads below
-  constexpr int KV = D * static_cast<int>(sizeof(T)) / 16;  // vectors per row
-  constexpr int KPRE = KV <= 16 ? KV : 16;                    // preloaded vectors
-  constexpr int EV = 16 / static_cast<int>(sizeof(T));        // elements per vector
-  const int kj = c0 + tid;
-  uint4 kreg[KPRE];
-  const uint4* krow = reinterpret_cast<const uint4*>(K + static_cast<size_t>(kj < L ? kj : c0) * D);
-#pragma unroll
-  for (int i = 0; i < KPRE; ++i) kreg[i] = __ldg(krow + i);
-  // this chunk of V (rows past L read as zero)
-  for (int e = tid; e < kChunk * KV; e += kChunk) {
-    const int row = e / KV, col = (e % KV) * EV;
-    uint4 u = make_uint4(0u, 0u, 0u, 0u);
-    if (c0 + row < L)
-      u = __ldg(reinterpret_cast<const uint4*>(V + static_cast<size_t>(c0 + row) * D + col));
-    *reinterpret_cast<uint4*>(v_s + row * D + col) = u;
+  const int nvc = (L + kChunk - 1) / kChunk;  // chunks holding valid rows
+  const int cb = split * a.cps;
+  const int ce = min(cb + a.cps, nvc);
+  if (cb >= ce) return;  // past this element's cache: the combine skips the split
+  const int n = ce - cb;
+  volatile int* abort = &abort_sh;
+  auto sK = [&](int s) { return smem + 2 * s * TILE; };
+  auto sV = [&](int s) { return smem + (2 * s + 1) * TILE; };
+  auto issue = [&](int it) {  // thread 0: chunk cb + it into stage it % STAGES
+    const int s = it % STAGES;
+    const uint32_t bar = smem_u32(&full[s]);
+    mbar_expect_tx(bar, 2 * TILE);
+    for (int k = 0; k < NBLK; ++k) {
+      tma_load_3d(smem_u32(sK(s) + k * BLK), &a.tmK, bar, k * (128 / ES), (cb + it) * kChunk, bg);
+      tma_load_3d(smem_u32(sV(s) + k * BLK), &a.tmV, bar, k * (128 / ES), (cb + it) * kChunk, bg);
+    }
+  };
+  if (tid == 0) {
+    abort_sh = 0;
+    for (int s = 0; s < STAGES; ++s) mbar_init(smem_u32(&full[s]), 1);
+    fence_barrier_init();
+    prefetch_tmap(&a.tmK);
+    prefetch_tmap(&a.tmV);
   }
+  __syncthreads();
+  int issued = 0;  // chunks whose loads thread 0 has issued
+  if (tid == 0)
+    for (; issued < STAGES && issued < n; ++issued) issue(issued);
   // query rows r = gi * nq + t of heads g*G + gi (absent rows: zeros)
+  const T* Q = static_cast<const T*>(a.Q);
+  const float cq = a.scale * kLog2e;
   for (int e = tid; e < RM * D; e += kChunk) {
     const int r = e / D, k = e % D, gi = r / a.nq, t = r % a.nq;
     float x = 0.f;
     if (r < R) x = to_f(Q[((static_cast<size_t>(b) * a.H + g * G + gi) * a.nq + t) * D + k]) * cq;
     q_s[e] = x;
   }
-  __syncthreads();
-  // scores of this thread's cache row against the RM rows: packed fp32
-  // FMAs over element pairs, the two halves summed at the end
-  float2 acc2[RM];
+  // P V ownership: rows warp + 4 i, columns CPL * lane .. + CPL (its place in a swizzled row)
+  constexpr int RW = RM / 4;
+  constexpr int CPL = D / 32;
+  const int cbyte = CPL * lane * ES;
+  const int vblk = cbyte / 128, vchunk = (cbyte % 128) / 16, voff = cbyte % 16;
+  float2 o[RW][CPL / 2];
+  float m_run[RW], l_run[RW];
 #pragma unroll
-  for (int r = 0; r < RM; ++r) acc2[r] = make_float2(0.f, 0.f);
+  for (int i = 0; i < RW; ++i) {
+    m_run[i] = -INFINITY;
+    l_run[i] = 0.f;
 #pragma unroll
-  for (int part = 0; part < KV / KPRE; ++part) {
-    if (part > 0) {
+    for (int cc = 0; cc < CPL / 2; ++cc) o[i][cc] = make_float2(0.f, 0.f);
+  }
+  bool ok = true;
+  for (int it = 0; it < n; ++it) {
+    const int s = it % STAGES;
+    const int c0 = (cb + it) * kChunk;
+    const int jmax = min(kChunk, L - c0);  // valid rows of this chunk
+    // every thread waits itself; the CTA agrees before it goes on
+    ok = __syncthreads_and(mbar_wait(smem_u32(&full[s]), (it / STAGES) & 1, abort, 90, a.status));
+    if (!ok) break;
+    // scores of cache row c0 + tid, read from its swizzled row
+    const int r8 = tid & 7;
+    float2 acc2[RM];
 #pragma unroll
-      for (int i = 0; i < KPRE; ++i) kreg[i] = __ldg(krow + part * KPRE + i);
-    }
+    for (int r = 0; r < RM; ++r) acc2[r] = make_float2(0.f, 0.f);
+    const uint8_t* krow = sK(s) + tid * 128;
 #pragma unroll
-    for (int i = 0; i < KPRE; ++i) {
-      float kv[EV];
-      unpack(kreg[i], kv);
-      const int k0 = (part * KPRE + i) * EV;
+    for (int bl = 0; bl < NBLK; ++bl) {
 #pragma unroll
-      for (int r = 0; r < RM; ++r) {
-        if (r < R) {
-          float2 s = acc2[r];
+      for (int k = 0; k < 8; ++k) {
+        const uint4 u = *reinterpret_cast<const uint4*>(krow + bl * BLK + ((k ^ r8) << 4));
+        float kv[EV];
+        unpack(u, kv);
+        const int e0 = (bl * 128 + k * 16) / ES;
 #pragma unroll
-          for (int k4 = 0; k4 < EV; k4 += 4) {
-            const float4 qv = *reinterpret_cast<const float4*>(q_s + r * D + k0 + k4);
-            s = __ffma2_rn(make_float2(qv.x, qv.y), make_float2(kv[k4], kv[k4 + 1]), s);
-            s = __ffma2_rn(make_float2(qv.z, qv.w), make_float2(kv[k4 + 2], kv[k4 + 3]), s);
+        for (int r = 0; r < RM; ++r) {
+          if (r < R) {
+            float2 sacc = acc2[r];
+#pragma unroll
+            for (int k4 = 0; k4 < EV; k4 += 4) {
+              const float4 qv = *reinterpret_cast<const float4*>(q_s + r * D + e0 + k4);
+              sacc = __ffma2_rn(make_float2(qv.x, qv.y), make_float2(kv[k4], kv[k4 + 1]), sacc);
+              sacc = __ffma2_rn(make_float2(qv.z, qv.w), make_float2(kv[k4 + 2], kv[k4 + 3]), sacc);
+            }
+            acc2[r] = sacc;
           }
-          acc2[r] = s;
         }
       }
     }
-  }
-  float acc[RM];
+    // rows past L may hold anything: zero their V so that P V stays finite
+    if (tid >= jmax) {
+      uint8_t* vrow = sV(s) + tid * 128;
 #pragma unroll
-  for (int r = 0; r < RM; ++r) acc[r] = acc2[r].x + acc2[r].y;
-  // masked scores; the chunk's max per row (warp shuffles, then across warps)
+      for (int bl = 0; bl < NBLK; ++bl)
 #pragma unroll
-  for (int r = 0; r < RM; ++r) {
-    const int pos = L - a.nq + r % a.nq;  // this row's token position
-    float sv = (r < R && kj < L && kj <= pos) ? acc[r] : -INFINITY;
-    acc[r] = sv;
+        for (int k = 0; k < 8; ++k)
+          *reinterpret_cast<uint4*>(vrow + bl * BLK + (k << 4)) = make_uint4(0u, 0u, 0u, 0u);
+      fence_proxy_async();  // ordered before the TMA that refills this stage
+    }
+    const int kj = c0 + tid;
+    float sc[RM];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sv = fmaxf(sv, __shfl_xor_sync(0xffffffffu, sv, off));
-    if (lane == 0) red[warp * RM + r] = sv;
-  }
-  __syncthreads();
+    for (int r = 0; r < RM; ++r) {
+      const int pos = L - a.nq + r % a.nq;  // this row's token position
+      float sv = (r < R && tid < jmax && kj <= pos) ? acc2[r].x + acc2[r].y : -INFINITY;
+      sc[r] = sv;
 #pragma unroll
-  for (int r = 0; r < RM; ++r) {
-    const float m = fmaxf(fmaxf(red[r], red[RM + r]), fmaxf(red[2 * RM + r], red[3 * RM + r]));
-    float p = m == -INFINITY ? 0.f : exp2f(acc[r] - m);
-    p_s[r * kChunk + tid] = p;
+      for (int off = 16; off > 0; off >>= 1) sv = fmaxf(sv, __shfl_xor_sync(0xffffffffu, sv, off));
+      if (lane == 0) red[warp * RM + r] = sv;
+    }
+    __syncthreads();
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
-    if (lane == 0) red[4 * RM + warp * RM + r] = p;
-    acc[r] = m;
-  }
-  __syncthreads();
-  // partial O = P V: warp w takes rows w, w + 4, ...; lane l the CPL columns
-  // from CPL * l, over all kChunk rows of the chunk
-  constexpr int RW = RM / 4;   // rows per warp
-  constexpr int CPL = D / 32;  // columns per lane
-  float2 o[RW][CPL / 2];
+    for (int r = 0; r < RM; ++r) {
+      const float m = fmaxf(fmaxf(red[r], red[RM + r]), fmaxf(red[2 * RM + r], red[3 * RM + r]));
+      float p = m == -INFINITY ? 0.f : exp2f(sc[r] - m);
+      p_s[r * kChunk + tid] = p;
 #pragma unroll
-  for (int i = 0; i < RW; ++i)
+      for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
+      if (lane == 0) red[4 * RM + warp * RM + r] = p;
+    }
+    __syncthreads();
+    // fold this chunk into the running (max, sum, O) of the warp's rows
+    float2 oc[RW][CPL / 2];
 #pragma unroll
-    for (int cc = 0; cc < CPL / 2; ++cc) o[i][cc] = make_float2(0.f, 0.f);
-  const bool any = warp < R;  // this warp owns at least one present row
-  if (any) {
+    for (int i = 0; i < RW; ++i)
+#pragma unroll
+      for (int cc = 0; cc < CPL / 2; ++cc) oc[i][cc] = make_float2(0.f, 0.f);
+    const uint8_t* vcol = sV(s) + vblk * BLK + voff;
+    if constexpr (RM == 4) {
+      // few rows: warp w takes keys 32w .. 32w + 31 for every row, so each V
+      // element is read once; the four warps' partials meet in shared memory
+      float2 ok4[4][CPL / 2];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int cc = 0; cc < CPL / 2; ++cc) ok4[r][cc] = make_float2(0.f, 0.f);
 #pragma unroll 2
-    for (int j = 0; j < kChunk; j += 4) {
-      float pv[RW][4];
+      for (int j = 32 * warp; j < 32 * warp + 32; j += 4) {
+        float pv[4][4];
 #pragma unroll
-      for (int i = 0; i < RW; ++i) {
-        const float4 x = *reinterpret_cast<const float4*>(p_s + (warp + 4 * i) * kChunk + j);
-        pv[i][0] = x.x; pv[i][1] = x.y; pv[i][2] = x.z; pv[i][3] = x.w;
+        for (int r = 0; r < 4; ++r) {
+          const float4 x = *reinterpret_cast<const float4*>(p_s + r * kChunk + j);
+          pv[r][0] = x.x; pv[r][1] = x.y; pv[r][2] = x.z; pv[r][3] = x.w;
+        }
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int row = j + jj;
+          float vv[CPL];
+          load_cols<CPL>(reinterpret_cast<const T*>(vcol + row * 128 + ((vchunk ^ (row & 7)) << 4)), vv);
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+            if (r < R)
+#pragma unroll
+              for (int cc = 0; cc < CPL / 2; ++cc)
+                ok4[r][cc] = __ffma2_rn(make_float2(pv[r][jj], pv[r][jj]),
+                                        make_float2(vv[2 * cc], vv[2 * cc + 1]), ok4[r][cc]);
+        }
       }
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        float vv[CPL];
-        load_cols<CPL>(v_s + (j + jj) * D + CPL * lane, vv);
+      for (int r = 0; r < 4; ++r)
 #pragma unroll
-        for (int i = 0; i < RW; ++i)
+        for (int cc = 0; cc < CPL / 2; ++cc)
+          *reinterpret_cast<float2*>(red_o + (warp * 4 + r) * D + CPL * lane + 2 * cc) = ok4[r][cc];
+      __syncthreads();
 #pragma unroll
-          for (int cc = 0; cc < CPL / 2; ++cc)
-            o[i][cc] = __ffma2_rn(make_float2(pv[i][jj], pv[i][jj]),
-                                  make_float2(vv[2 * cc], vv[2 * cc + 1]), o[i][cc]);
+      for (int cc = 0; cc < CPL / 2; ++cc)
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const float2 x = *reinterpret_cast<const float2*>(red_o + (w * 4 + warp) * D + CPL * lane + 2 * cc);
+          oc[0][cc].x += x.x;
+          oc[0][cc].y += x.y;
+        }
+    } else if (warp < R) {
+#pragma unroll 2
+      for (int j = 0; j < kChunk; j += 4) {
+        float pv[RW][4];
+#pragma unroll
+        for (int i = 0; i < RW; ++i) {
+          const float4 x = *reinterpret_cast<const float4*>(p_s + (warp + 4 * i) * kChunk + j);
+          pv[i][0] = x.x; pv[i][1] = x.y; pv[i][2] = x.z; pv[i][3] = x.w;
+        }
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int row = j + jj;
+          float vv[CPL];
+          load_cols<CPL>(reinterpret_cast<const T*>(vcol + row * 128 + ((vchunk ^ (row & 7)) << 4)), vv);
+#pragma unroll
+          for (int i = 0; i < RW; ++i)
+#pragma unroll
+            for (int cc = 0; cc < CPL / 2; ++cc)
+              oc[i][cc] = __ffma2_rn(make_float2(pv[i][jj], pv[i][jj]),
+                                     make_float2(vv[2 * cc], vv[2 * cc + 1]), oc[i][cc]);
+        }
       }
     }
+    if (warp < R) {
+#pragma unroll
+      for (int i = 0; i < RW; ++i) {
+        const int r = warp + 4 * i;
+        const float mc = fmaxf(fmaxf(red[r], red[RM + r]), fmaxf(red[2 * RM + r], red[3 * RM + r]));
+        const float* ps = red + 4 * RM;
+        const float lc = ps[r] + ps[RM + r] + ps[2 * RM + r] + ps[3 * RM + r];
+        const float mn = fmaxf(m_run[i], mc);
+        const float al = mn == -INFINITY ? 1.f : exp2f(m_run[i] - mn);
+        const float be = mn == -INFINITY ? 0.f : exp2f(mc - mn);
+#pragma unroll
+        for (int cc = 0; cc < CPL / 2; ++cc)
+          o[i][cc] = __ffma2_rn(o[i][cc], make_float2(al, al),
+                                __fmul2_rn(oc[i][cc], make_float2(be, be)));
+        l_run[i] = fmaf(l_run[i], al, be * lc);
+        m_run[i] = mn;
+      }
+    }
+    __syncthreads();  // stage s fully read: refill it
+    if (tid == 0 && issued < n) issue(issued++);
+  }
+  if (!ok) {
+    // unwinding: let this CTA's copies land before it exits
+    if (tid == 0)
+      for (int it = issued > STAGES ? issued - STAGES : 0; it < issued; ++it)
+        mbar_wait_drain(smem_u32(&full[it % STAGES]), (it / STAGES) & 1, 91, a.status);
+    return;
   }
 #pragma unroll
   for (int i = 0; i < RW; ++i) {
@@ -221,18 +342,13 @@ __global__ void __launch_bounds__(kChunk) decode_partial_kernel(const DecodeArgs
     if (r < R) {
       const int gi = r / a.nq, t = r % a.nq;
       const size_t row = (static_cast<size_t>(b) * a.H + g * G + gi) * a.nq + t;
-      float* dst = a.opart + (row * a.nchunk + c) * D + CPL * lane;
+      float* dst = a.opart + (row * a.nchunk + split) * D + CPL * lane;
 #pragma unroll
       for (int cc = 0; cc < CPL / 2; ++cc) {
         dst[2 * cc] = o[i][cc].x;
         dst[2 * cc + 1] = o[i][cc].y;
       }
-      if (lane == 0) {
-        const float* ps = red + 4 * RM;
-        const float l = ps[r] + ps[RM + r] + ps[2 * RM + r] + ps[3 * RM + r];
-        const float m = fmaxf(fmaxf(red[r], red[RM + r]), fmaxf(red[2 * RM + r], red[3 * RM + r]));
-        a.ml[row * a.nchunk + c] = make_float2(m, l);
-      }
+      if (lane == 0) a.ml[row * a.nchunk + split] = make_float2(m_run[i], l_run[i]);
     }
   }
 }
@@ -252,7 +368,7 @@ __global__ void __launch_bounds__(kCombine) decode_combine_kernel(const DecodeAr
   const int tid = threadIdx.x, col = tid % D, grp = tid / D;
   const int b = static_cast<int>(row / (static_cast<long long>(a.H) * a.nq));
   const int L = cache_len(a, b);
-  const int nc = (L + kChunk - 1) / kChunk;
+  const int nc = ((L + kChunk - 1) / kChunk + a.cps - 1) / a.cps;  // splits with valid rows
   const float2* ml = a.ml + row * a.nchunk;
   // common max over the chunks
   float M = -INFINITY;
@@ -288,23 +404,39 @@ __global__ void __launch_bounds__(kCombine) decode_combine_kernel(const DecodeAr
   }
 }
 
+// Splits: as many CTAs as fit on the GPU at once (one wave), at most one
+// per chunk; each streams its run of chunks.  `a` arrives with nchunk = the
+// number of chunks (the workspace's capacity) and leaves with the split
+// count and chunks per split that both kernels use.
 template <typename T, int D, int RM>
-cudaError_t launch_partial(const DecodeArgs& a, cudaStream_t stream) {
-  const int smem = (RM * D + RM * kChunk + 8 * RM) * 4 + kChunk * D * static_cast<int>(sizeof(T));
-  auto kp = decode_partial_kernel<T, D, RM>;
+cudaError_t launch_partial(DecodeArgs& a, int sms, cudaStream_t stream) {
+  constexpr int TILE = kChunk * D * static_cast<int>(sizeof(T));
+  constexpr int STAGES = 4 * TILE <= 160 * 1024 ? 2 : 1;  // fp32 d = 128: one stage
+  const int smem = 1024 + 2 * STAGES * TILE + (RM * D + RM * kChunk + 8 * RM) * 4 +
+                   (RM == 4 ? 16 * D * 4 : 0);
+  auto kp = decode_partial_kernel<T, D, RM, STAGES>;
   cudaError_t e = cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  int per_sm = 1;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kp, kChunk, smem);
+  if (e != cudaSuccess) return e;
+  const long long bg = static_cast<long long>(a.B) * a.Hkv;
+  const long long slots = static_cast<long long>(per_sm > 0 ? per_sm : 1) * sms;
+  const int chunks = a.nchunk;
+  const int nsplit = static_cast<int>(std::min<long long>(chunks, std::max<long long>(1, slots / bg)));
+  a.cps = (chunks + nsplit - 1) / nsplit;
+  a.nchunk = (chunks + a.cps - 1) / a.cps;
   kp<<<dim3(a.nchunk, a.B * a.Hkv), kChunk, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
 template <typename T, int D>
-cudaError_t launch_t(const DecodeArgs& a, cudaStream_t stream) {
+cudaError_t launch_t(DecodeArgs a, int sms, cudaStream_t stream) {
   const int R = (a.H / a.Hkv) * a.nq;
-  cudaError_t e = R <= 4    ? launch_partial<T, D, 4>(a, stream)
-                  : R <= 8  ? launch_partial<T, D, 8>(a, stream)
-                  : R <= 16 ? launch_partial<T, D, 16>(a, stream)
-                            : launch_partial<T, D, kMaxDecodeRows>(a, stream);
+  cudaError_t e = R <= 4    ? launch_partial<T, D, 4>(a, sms, stream)
+                  : R <= 8  ? launch_partial<T, D, 8>(a, sms, stream)
+                  : R <= 16 ? launch_partial<T, D, 16>(a, sms, stream)
+                            : launch_partial<T, D, kMaxDecodeRows>(a, sms, stream);
   if (e != cudaSuccess) return e;
   const long long rows = static_cast<long long>(a.B) * a.H * a.nq;
   decode_combine_kernel<T, D><<<static_cast<unsigned>(rows), kCombine, 0, stream>>>(a);
@@ -315,11 +447,11 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t stream) {
 
 int decode_chunk_rows() { return kChunk; }
 
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
-  if (a.dtype == 0 && a.d == 64) return launch_t<__nv_bfloat16, 64>(a, stream);
-  if (a.dtype == 0 && a.d == 128) return launch_t<__nv_bfloat16, 128>(a, stream);
-  if (a.dtype == 1 && a.d == 64) return launch_t<float, 64>(a, stream);
-  if (a.dtype == 1 && a.d == 128) return launch_t<float, 128>(a, stream);
+cudaError_t launch_decode(const DecodeArgs& a, int sms, cudaStream_t stream) {
+  if (a.dtype == 0 && a.d == 64) return launch_t<__nv_bfloat16, 64>(a, sms, stream);
+  if (a.dtype == 0 && a.d == 128) return launch_t<__nv_bfloat16, 128>(a, sms, stream);
+  if (a.dtype == 1 && a.d == 64) return launch_t<float, 64>(a, sms, stream);
+  if (a.dtype == 1 && a.d == 128) return launch_t<float, 128>(a, sms, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -1,5 +1,6 @@
 // nea_api.cu -- the C ABI declared in include/nea_attn.h: argument checks,
 // TMA descriptor encoding, workspace carving, launches, device status word.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -41,6 +42,21 @@ EncodeTiledFn encoder() {
     g_encode = reinterpret_cast<EncodeTiledFn>(fn);
   }
   return g_encode;
+}
+
+// Number of SMs of the current device (cached per device).
+int sm_count() {
+  static int cache[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+      n = 1;
+    cache[dev] = n;
+  }
+  return cache[dev];
 }
 
 // Device address of g_status_word on the current device.
@@ -402,17 +418,28 @@ int nea_attn_decode(const void* Q, const void* Kc, const void* Vc, const int* le
   DecodeArgs a;
   std::memset(&a, 0, sizeof(a));
   const size_t rows = static_cast<size_t>(B) * H * nq;
-  a.nchunk = (Lmax + decode_chunk_rows() - 1) / decode_chunk_rows();
+  const int chunks = (Lmax + decode_chunk_rows() - 1) / decode_chunk_rows();
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.opart = reinterpret_cast<float*>(ws);
-  a.ml = reinterpret_cast<float2*>(ws + align256(rows * a.nchunk * d * sizeof(float)));
+  a.ml = reinterpret_cast<float2*>(ws + align256(rows * chunks * d * sizeof(float)));
+  // the launcher splits the chunks over one wave of CTAs; the workspace holds
+  // one split per chunk, the most it can choose
+  a.nchunk = chunks;
+  a.cps = 1;
+  const long long bg = static_cast<long long>(B) * Hkv;
+  const CUtensorMapDataType dt =
+      dtype == NEA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const int es = dtype == NEA_BF16 ? 2 : 4;
+  if (!encode_3d(&a.tmK, Kc, dt, es, d, Lmax, bg) || !encode_3d(&a.tmV, Vc, dt, es, d, Lmax, bg))
+    return NEA_ERR_CUDA;
   a.Q = Q; a.Kc = Kc; a.Vc = Vc; a.lens = lens; a.O = O; a.lse = LSE;
   a.status = status_ptr();
   if (!a.status) return NEA_ERR_CUDA;
   a.B = B; a.H = H; a.Hkv = Hkv; a.nq = nq; a.Lmax = Lmax; a.d = d; a.dtype = dtype;
   a.scale = scale;
-  return launch_decode(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? NEA_OK
-                                                                           : NEA_ERR_CUDA;
+  return launch_decode(a, sm_count(), static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? NEA_OK
+             : NEA_ERR_CUDA;
 }
 
 int nea_attn_check_status(void* stream) {

@@ -50,16 +50,20 @@ struct BwdArgs {
 constexpr int kMaxDecodeRows = 32;  // G * nq query rows per KV head at most
 constexpr unsigned int kStatusBadLength = 2u;  // a cache length outside [nq, Lmax]
 struct DecodeArgs {
+  CUtensorMap tmK, tmV;  // caches as {d, Lmax, B*Hkv}, boxes of 128 B x 128 rows, 128-B swizzle
   const void* Q;       // [B][H][nq][d] dtype
   const void* Kc;      // [B][Hkv][Lmax][d] dtype
   const void* Vc;
   const int* lens;     // [B] valid cache rows per batch element (device)
   void* O;             // [B][H][nq][d] dtype
   float* lse;          // [B][H][nq]
-  float* opart;        // workspace: [B*H*nq][nchunk][d] partial P V
-  float2* ml;          // workspace: [B*H*nq][nchunk] (max, sum) per chunk
+  float* opart;        // workspace: [B*H*nq][nchunk][d] partial P V per split
+  float2* ml;          // workspace: [B*H*nq][nchunk] (max, sum) per split
   unsigned int* status;
-  int B, H, Hkv, nq, Lmax, d, nchunk, dtype;
+  int B, H, Hkv, nq, Lmax, d, dtype;
+  int nchunk;          // splits of the cache per (batch, KV head), one CTA each (the
+                       // launcher sets it from the chunk count it receives here)
+  int cps;             // 128-row chunks per split (set by the launcher)
   float scale;
 };
 int decode_chunk_rows();
@@ -79,7 +83,7 @@ cudaError_t launch_bwd_main_f32(const BwdArgs& a, const CUtensorMap& tmQt,
                                 const CUtensorMap& tmdOt, const CUtensorMap& tmKt,
                                 cudaStream_t stream);
 // Rotary embedding: the (cos, sin) table [N][d/2], and Qr = R(Q), Kr = R(K).
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeArgs& a, int sms, cudaStream_t stream);
 cudaError_t launch_rope_table(float2* cs, int N, int d, double base, cudaStream_t stream);
 cudaError_t launch_rope_rotate(const void* Q, const void* K, void* Qr, void* Kr,
                                const float2* cs, long long qrows, long long krows, int N, int d,

@@ -42,11 +42,13 @@ constexpr float kLog2e = 1.4426950408889634f;
 // L2 = LSE * log2(e); padding rows get Ds = 0 and L2 = +inf, so that the main
 // kernel's exp2(S c - L2) is exactly 0 for them.  TPR threads per row, each
 // owning 16 bytes of O and dO; every thread handles kPreRows rows with all
-// loads issued before any use.
+// loads (the row's LSE included) issued before any use, so that a wave of
+// blocks waits for memory once.
 constexpr int kPreRows = 4;
+constexpr int kPreThreads = 256;
 
 template <typename T, int D>
-__global__ void __launch_bounds__(256) bwd_pre_kernel(const T* __restrict__ O,
+__global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const T* __restrict__ O,
                                                       const T* __restrict__ dO,
                                                       const float* __restrict__ lse,
                                                       float* __restrict__ ds_row,
@@ -55,7 +57,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const T* __restrict__ O,
                                                       int N, int npad, float scale) {
   constexpr int EPV = 16 / sizeof(T);  // elements per 16-B vector
   constexpr int TPR = D / EPV;         // threads per row
-  constexpr int RPB = 256 / TPR;       // rows per block per pass
+  constexpr int RPB = kPreThreads / TPR;  // rows per block per pass
   static_assert(kTile % (RPB * kPreRows) == 0, "a block's rows must divide a tile");
   const int sub = threadIdx.x % TPR;
   // A block's RPB * kPreRows rows divide npad (a multiple of 128), so the
@@ -65,16 +67,19 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const T* __restrict__ O,
   const int nb = static_cast<int>(pb - bh * npad) + threadIdx.x / TPR;
   const long long p0 = pb + threadIdx.x / TPR;
   uint4 ov[kPreRows], gv[kPreRows];
+  float lv[kPreRows];
   long long rrow[kPreRows];  // unpadded row index, or -1 for padding / past the end
 #pragma unroll
   for (int u = 0; u < kPreRows; ++u) {
     const long long p = p0 + static_cast<long long>(u) * RPB;
     const int n = nb + u * RPB;
     rrow[u] = (p < prows && n < N) ? bh * N + n : -1;
+    lv[u] = 0.f;
     if (rrow[u] >= 0) {
       const size_t base = static_cast<size_t>(rrow[u]) * D + sub * EPV;
       ov[u] = __ldg(reinterpret_cast<const uint4*>(O + base));
       gv[u] = __ldg(reinterpret_cast<const uint4*>(dO + base));
+      if (sub == 0) lv[u] = __ldg(lse + rrow[u]);
     } else {
       ov[u] = gv[u] = make_uint4(0, 0, 0, 0);
     }
@@ -103,7 +108,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const T* __restrict__ O,
     for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (p < prows && sub == 0) {
       ds_row[p] = rrow[u] >= 0 ? acc * scale : 0.f;
-      l2_row[p] = rrow[u] >= 0 ? lse[rrow[u]] * kLog2e : INFINITY;
+      l2_row[p] = rrow[u] >= 0 ? lv[u] * kLog2e : INFINITY;
     }
     // zero this thread's share of the fp32 accumulator row (D floats)
     if (dq_acc != nullptr && rrow[u] >= 0) {
@@ -118,17 +123,18 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const T* __restrict__ O,
 // Each thread converts kPostVecs groups of 8 fp32 -> 8 bf16.  With a RoPE
 // table, the 4 pairs of a group are first turned back by their row's angles.
 constexpr int kPostVecs = 4;
+constexpr int kPostThreads = 256;
 
-__global__ void __launch_bounds__(256) bwd_post_kernel(const float* __restrict__ acc,
+__global__ void __launch_bounds__(kPostThreads) bwd_post_kernel(const float* __restrict__ acc,
                                                        __nv_bfloat16* __restrict__ dq,
                                                        long long n8,
                                                        const float2* __restrict__ cs, int N,
                                                        int d) {
-  const long long i0 = static_cast<long long>(blockIdx.x) * 256 * kPostVecs + threadIdx.x;
+  const long long i0 = static_cast<long long>(blockIdx.x) * kPostThreads * kPostVecs + threadIdx.x;
   float4 a[kPostVecs], b[kPostVecs];
 #pragma unroll
   for (int u = 0; u < kPostVecs; ++u) {
-    const long long i = i0 + static_cast<long long>(u) * 256;
+    const long long i = i0 + static_cast<long long>(u) * kPostThreads;
     if (i < n8) {
       a[u] = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i);
       b[u] = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i + 1);
@@ -137,7 +143,7 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const float* __restrict__
   if (cs != nullptr) {
 #pragma unroll
     for (int u = 0; u < kPostVecs; ++u) {
-      const long long i = i0 + static_cast<long long>(u) * 256;
+      const long long i = i0 + static_cast<long long>(u) * kPostThreads;
       if (i < n8) {
         const long long e = 8 * i;  // first element of the group; d % 8 == 0
         const long long row = e / d;
@@ -152,7 +158,7 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const float* __restrict__
   }
 #pragma unroll
   for (int u = 0; u < kPostVecs; ++u) {
-    const long long i = i0 + static_cast<long long>(u) * 256;
+    const long long i = i0 + static_cast<long long>(u) * kPostThreads;
     if (i < n8) {
       uint4 v;
       v.x = pack_bf16(a[u].x, a[u].y);
@@ -643,18 +649,18 @@ cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t stream) {
   const long long prows = static_cast<long long>(a.B) * a.H * npad;
   const int esize = a.dtype == 0 ? 2 : 4;
   const int tpr = a.d * esize / 16;
-  const long long per_block = static_cast<long long>(256 / tpr) * kPreRows;  // divides 128
+  const long long per_block = static_cast<long long>(kPreThreads / tpr) * kPreRows;  // divides 128
   const unsigned grid = static_cast<unsigned>((prows + per_block - 1) / per_block);
   if (a.dtype == 0 && a.d == 64)
-    bwd_pre_kernel<__nv_bfloat16, 64><<<grid, 256, 0, stream>>>(
+    bwd_pre_kernel<__nv_bfloat16, 64><<<grid, kPreThreads, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(a.O), static_cast<const __nv_bfloat16*>(a.dO), a.lse,
         a.delta, a.lse2, a.dq_acc, prows, a.N, npad, a.scale);
   else if (a.dtype == 0 && a.d == 128)
-    bwd_pre_kernel<__nv_bfloat16, 128><<<grid, 256, 0, stream>>>(
+    bwd_pre_kernel<__nv_bfloat16, 128><<<grid, kPreThreads, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(a.O), static_cast<const __nv_bfloat16*>(a.dO), a.lse,
         a.delta, a.lse2, a.dq_acc, prows, a.N, npad, a.scale);
   else if (a.dtype == 1 && a.d == 64)
-    bwd_pre_kernel<float, 64><<<grid, 256, 0, stream>>>(
+    bwd_pre_kernel<float, 64><<<grid, kPreThreads, 0, stream>>>(
         static_cast<const float*>(a.O), static_cast<const float*>(a.dO), a.lse, a.delta, a.lse2,
         a.dq_acc, prows, a.N, npad, a.scale);
   else
@@ -673,8 +679,9 @@ cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_bwd_post(const BwdArgs& a, cudaStream_t stream) {
   const long long n8 = static_cast<long long>(a.B) * a.H * a.N * a.d / 8;
-  const long long per_block = 256LL * kPostVecs;
-  bwd_post_kernel<<<static_cast<unsigned>((n8 + per_block - 1) / per_block), 256, 0, stream>>>(
+  const long long per_block = static_cast<long long>(kPostThreads) * kPostVecs;
+  bwd_post_kernel<<<static_cast<unsigned>((n8 + per_block - 1) / per_block), kPostThreads, 0,
+                    stream>>>(
       a.dq_acc, static_cast<__nv_bfloat16*>(a.dQ), n8, a.rope_cs, a.N, a.d);
   return cudaGetLastError();
 }

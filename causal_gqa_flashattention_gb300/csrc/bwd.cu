@@ -543,11 +543,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
           (static_cast<size_t>(b) * a.Hkv + g) * a.N + static_cast<size_t>(j) * kTile + kr;
       __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(half == 0 ? a.dV : a.dK) + row * D;
       const uint32_t col = half == 0 ? C::DV_COL : C::DK_COL;
+#pragma unroll
       // dK of rotated keys -> dK of the caller's keys (RoPE)
       const float2* rcs = (half == 1 && row_ok && a.rope_cs != nullptr)
                               ? a.rope_cs + static_cast<size_t>(j * kTile + kr) * (D / 2)
                               : nullptr;
-#pragma unroll
       for (int cc = 0; cc < D; cc += 32) {
         uint32_t v[32];
         tmem_ld32(trow + col + cc, v);

@@ -117,9 +117,13 @@ int check_common(int B, int H, int Hkv, int N, int d, float scale, int causal, i
   if (causal != 0 && causal != 1) return NEA_ERR_INVALID;
   if (dtype != NEA_BF16 && dtype != NEA_F32) return NEA_ERR_INVALID;
   if (!std::isfinite(scale) || !(scale > 0.f)) return NEA_ERR_INVALID;
-  // Grid and TMA coordinate ranges: B*H*(N/128) CTAs, heads and rows as int.
+  // Grid and TMA coordinate ranges: heads and rows as int, and at most
+  // B*H*ceil(N/128) CTAs in one grid dimension.
   const long long bh = static_cast<long long>(B) * H;
   if (bh > (1LL << 24) || N > (1 << 24)) return NEA_ERR_UNSUPPORTED;
+  if (bh * ((N + kTile - 1) / kTile) > 0x7fffffffLL) return NEA_ERR_UNSUPPORTED;
+  // element-wise kernels (dQ cast, RoPE) launch one thread per 8..32 elements
+  if (bh * N > (1LL << 40) / d) return NEA_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return NEA_ERR_UNSUPPORTED;
   (void)bwd;
   if (dtype == NEA_F32 && d != 64) return NEA_ERR_UNSUPPORTED;

@@ -71,7 +71,7 @@ def bwd(nea, ptrs=None, ws=P, ws_bytes=1 << 40, **kw):
     (dict(H=12, Hkv=5), -1), (dict(B=0), -1), (dict(N=0), -1), (dict(d=0), -1),
     (dict(causal=2), -1), (dict(dtype=3), -1), (dict(scale=0.0), -1),
     (dict(scale=float("nan")), -1), (dict(scale=float("inf")), -1), (dict(scale=-1.0), -1),
-    (dict(d=96), -2), (dict(d=32), -2),
+    (dict(d=96), -2), (dict(d=32), -2), (dict(B=1 << 14, H=1 << 10, Hkv=1 << 10, N=1 << 24), -2),
     (dict(dtype=1, d=128), -2),
 ])
 def test_invalid_and_unsupported_arguments(nea, kw, code):

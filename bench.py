@@ -429,6 +429,17 @@ def measure_extras(nea, w, q, k, v, do, o, lse, wsp, l2_flush, stream, peak_hbm,
                       "peak_source": f"hbm_gbs of {src}"}
     out["bwd_rope"] = {"ms": round(t_br, 5), "ms_without_rope": round(t_b, 5),
                        "overhead_pct": round(100.0 * (t_br / t_b - 1.0), 2)}
+    # full (non-causal) attention at the same shape: twice the causal work
+    of, lf = torch.empty_like(o), torch.empty_like(lse)
+    t_ff = _time_ms(lambda: nea.attn_fwd(q, k, v, causal=False, out=of, lse=lf, stream=stream),
+                    l2_flush, stream, reps)
+    t_fb = _time_ms(lambda: nea.attn_bwd(q, k, v, of, do, lf, causal=False, dq=dq, dk=dk, dv=dv,
+                                         workspace=wsp, stream=stream), l2_flush, stream, reps)
+    full_flops = 2.0 * (w.fwd_flops() + w.bwd_flops())
+    out["full_attention"] = {"fwd_ms": round(t_ff, 5), "bwd_ms": round(t_fb, 5),
+                             "tflops": round(full_flops / ((t_ff + t_fb) * 1e-3) / 1e12, 1),
+                             "frac_of_peak": round(full_flops / ((t_ff + t_fb) * 1e-3) / 1e12 /
+                                                   float(load_peaks()[0]["bf16_tflops"]), 4)}
     for name, dw in DECODE_WORKLOADS.items():
         dq_, kc, vc, lens = make_decode_inputs(dw, seed=0, device=q.device)
         od = torch.empty_like(dq_)

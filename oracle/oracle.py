@@ -183,3 +183,57 @@ def attn_decode(q, k_cache, v_cache, lens, scale: float):
     if rc != 0:
         raise ValueError("oracle_attn_decode_f64 rejected its arguments")
     return o, lse
+
+
+def attn_bwd_dq_rows(q, k, v, do, rows, scale: float, causal: bool = True):
+    """dQ for selected query rows only, fp64, from the definitions (for
+    sequences too long for the full backward): for row i of head h
+    (group g = h / (H / Hkv)),
+        P_ij  = softmax_j(scale q_i . k_j) over j <= i (all j if not causal)
+        O_i   = sum_j P_ij v_j,   D_i = dO_i . O_i,   dP_ij = dO_i . v_j
+        dQ_i  = scale sum_j P_ij (dP_ij - D_i) k_j.
+    ``rows`` is a list of (b, h, i); returns an array [len(rows), d]."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    H, Hkv = q.shape[1], k.shape[1]
+    N = q.shape[2]
+    out = np.empty((len(rows), q.shape[3]))
+    for n, (b, h, i) in enumerate(rows):
+        g = h // (H // Hkv)
+        end = i + 1 if causal else N
+        K, V = k[b, g, :end], v[b, g, :end]
+        s = scale * (K @ q[b, h, i])
+        p = np.exp(s - s.max())
+        p /= p.sum()
+        o = p @ V
+        dp = V @ do[b, h, i]
+        ds = p * (dp - do[b, h, i] @ o)
+        out[n] = scale * (ds @ K)
+    return out
+
+
+def attn_bwd_dkdv_rows(q, k, v, do, rows, scale: float, causal: bool = True):
+    """dK and dV for selected key rows, fp64, from the definitions: for key
+    row j of KV head g, summed over the group's query heads h and the query
+    rows i that see it (i >= j under the causal mask),
+        dK_j = scale sum_{h, i} P_ij (dP_ij - D_i) q_i,   dV_j = sum_{h, i} P_ij dO_i,
+    each P_ij, D_i from row i's full softmax.  Cheap for the last key rows of
+    a causal sequence.  ``rows`` is a list of (b, g, j); returns (dK, dV),
+    each [len(rows), d]."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    H, Hkv, N, d = q.shape[1], k.shape[1], q.shape[2], q.shape[3]
+    G = H // Hkv
+    dk = np.zeros((len(rows), d))
+    dv = np.zeros((len(rows), d))
+    for n, (b, g, j) in enumerate(rows):
+        for h in range(g * G, (g + 1) * G):
+            for i in range(j if causal else 0, N):
+                end = i + 1 if causal else N
+                K, V = k[b, g, :end], v[b, g, :end]
+                s = scale * (K @ q[b, h, i])
+                p = np.exp(s - s.max())
+                p /= p.sum()
+                o = p @ V
+                dij = p[j] * (V[j] @ do[b, h, i] - do[b, h, i] @ o)
+                dk[n] += scale * dij * q[b, h, i]
+                dv[n] += p[j] * do[b, h, i]
+    return dk, dv

@@ -260,3 +260,30 @@ def test_rowdot_matches_einsum():
 def test_rejects_bad_group():
     with pytest.raises(ValueError):
         oracle.attn_fwd(rand(1, 3, 4, 8), rand(1, 2, 4, 8), rand(1, 2, 4, 8), 1.0, True)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_dq_rows_match_full_backward(causal):
+    """The per-row dQ (used for long sequences) equals the full backward."""
+    B, H, Hkv, N, d = 2, 6, 2, 37, 8
+    q, k, v, do = rand(B, H, N, d), rand(B, Hkv, N, d), rand(B, Hkv, N, d), rand(B, H, N, d)
+    s = 1 / math.sqrt(d)
+    dq, _, _ = oracle.attn_bwd(q, k, v, do, s, causal)
+    rows = [(0, 0, 0), (0, 5, 36), (1, 3, 17), (1, 1, 1), (0, 2, 30)]
+    got = oracle.attn_bwd_dq_rows(q, k, v, do, rows, s, causal)
+    for n, (b, h, i) in enumerate(rows):
+        np.testing.assert_allclose(got[n], dq[b, h, i], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_dkdv_rows_match_full_backward(causal):
+    """The per-key-row dK, dV (used for long sequences) equal the full backward."""
+    B, H, Hkv, N, d = 1, 6, 2, 29, 8
+    q, k, v, do = rand(B, H, N, d), rand(B, Hkv, N, d), rand(B, Hkv, N, d), rand(B, H, N, d)
+    s = 1 / math.sqrt(d)
+    _, dk, dv = oracle.attn_bwd(q, k, v, do, s, causal)
+    rows = [(0, 0, 28), (0, 1, 27), (0, 1, 0), (0, 0, 13)]
+    gk, gv = oracle.attn_bwd_dkdv_rows(q, k, v, do, rows, s, causal)
+    for n, (b, g, j) in enumerate(rows):
+        np.testing.assert_allclose(gk[n], dk[b, g, j], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(gv[n], dv[b, g, j], rtol=0, atol=1e-12)

@@ -145,3 +145,61 @@ def test_full_size_workloads(nea, name):
                                WORKLOADS["gpt2s_f32"]], ids=lambda w: w.name)
 def test_f32_forward_backward(nea, w):
     run_case(nea, w)
+
+
+# Maximum sizes: sequences too long for the full fp64 oracle are checked on
+# sampled outputs the oracle computes one by one (an O row is the decode
+# oracle with one new token at that position; a dQ row needs only its own
+# softmax; dK / dV rows of the last key rows need only the few queries that
+# see them) and on identities that hold at any size:
+# sum_j dV_j = sum over the group's heads and rows of dO, and sum_j dK_j = 0.
+LONG = [custom(1, 4, 1, 16384, 64), custom(1, 2, 1, 8192, 128, causal=False)]
+
+
+@pytest.mark.parametrize("w", LONG, ids=lambda w: w.name)
+def test_long_sequence_sampled(nea, w):
+    dev = torch.device("cuda:0")
+    q, k, v, do = make_inputs(w, seed=11, device=dev)
+    o, lse = nea.attn_fwd(q, k, v, causal=w.causal, scale=w.scale)
+    dq, dk, dv = nea.attn_bwd(q, k, v, o, do, lse, causal=w.causal, scale=w.scale)
+    torch.cuda.synchronize()
+    assert nea.check_status() == 0
+    assert finite(o, lse, dq, dk, dv)
+    qc, kc, vc, doc = q.cpu(), k.cpu(), v.cpu(), do.cpu()
+    G = w.H // w.Hkv
+    N = w.N
+    rng = np.random.default_rng(5)
+    picks = sorted({0, 1, 127, 128, 129, N // 2, N - 129, N - 2, N - 1} |
+                   set(int(x) for x in rng.integers(0, N, 12)))
+    rows = [(0, h, i) for i in picks for h in (0, w.H - 1)]
+    # forward rows
+    for (b, h, i) in rows:
+        g = h // G
+        L = i + 1 if w.causal else N
+        ro, rl = oracle.attn_decode(qc[b:b + 1, h:h + 1, i:i + 1], kc[b:b + 1, g:g + 1],
+                                    vc[b:b + 1, g:g + 1], [L], w.scale)
+        got = o[b, h, i].float().cpu().numpy().astype(np.float64)
+        assert np.abs(got - ro[0, 0, 0]).max() <= O_MAXABS, (h, i)
+        assert abs(float(lse[b, h, i]) - rl[0, 0, 0]) <= LSE_MAXABS, (h, i)
+    # dQ rows
+    rdq = oracle.attn_bwd_dq_rows(qc, kc, vc, doc, rows, w.scale, w.causal)
+    gdq = np.stack([dq[b, h, i].float().cpu().numpy() for (b, h, i) in rows]).astype(np.float64)
+    assert np.linalg.norm(gdq - rdq) / np.linalg.norm(rdq) <= GRAD_REL
+    # dK, dV rows (the last key rows: only the queries after them contribute)
+    if w.causal:
+        krows = [(0, g, j) for g in range(w.Hkv) for j in (N - 1, N - 2, N - 129)]
+        rdk, rdv = oracle.attn_bwd_dkdv_rows(qc, kc, vc, doc, krows, w.scale, True)
+        gdk = np.stack([dk[b, g, j].float().cpu().numpy() for (b, g, j) in krows]).astype(np.float64)
+        gdv = np.stack([dv[b, g, j].float().cpu().numpy() for (b, g, j) in krows]).astype(np.float64)
+        assert np.linalg.norm(gdk - rdk) / np.linalg.norm(rdk) <= GRAD_REL
+        assert np.linalg.norm(gdv - rdv) / np.linalg.norm(rdv) <= GRAD_REL
+    # identities over every key row
+    dv64 = dv.double().cpu().numpy()
+    dk64 = dk.double().cpu().numpy()
+    do64 = doc.double().numpy()
+    for g in range(w.Hkv):
+        want = do64[0, g * G:(g + 1) * G].sum(axis=(0, 1))
+        got = dv64[0, g].sum(axis=0)
+        assert np.linalg.norm(got - want) <= 1e-2 * np.linalg.norm(want)
+        scale_k = np.abs(dk64[0, g]).sum(axis=0)
+        assert np.all(np.abs(dk64[0, g].sum(axis=0)) <= 1e-2 * scale_k + 1e-6)

@@ -239,13 +239,14 @@ def run_cuda(args):
         flush.zero_()
         flush.view(torch.float32).sum()  # read-back (no copy): L2 left holding clean lines
 
-    def step(evs=None):
+    def step(evs=None, st=None):
+        st = stream if st is None else st
         if evs:
-            evs[0].record(stream)
-        nea.attn_fwd(q, k, v, causal=True, scale=w.scale, out=o, lse=lse, stream=stream)
+            evs[0].record(st)
+        nea.attn_fwd(q, k, v, causal=True, scale=w.scale, out=o, lse=lse, stream=st)
         nea.attn_bwd_stages(q, k, v, o, do, lse, dq, dk, dv, wsp, causal=True, scale=w.scale,
-                            stream=stream,
-                            between=(lambda i: evs[i + 1].record(stream)) if evs else None)
+                            stream=st,
+                            between=(lambda i: evs[i + 1].record(st)) if evs else None)
 
     for _ in range(args.warmup):
         l2_flush()
@@ -255,22 +256,61 @@ def run_cuda(args):
         raise RuntimeError("kernel status word set during warm-up")
 
     K = args.steps
+    # The step's four kernels captured once as a CUDA graph (the same kernels
+    # and arguments; replays skip the per-launch host work and the gaps
+    # between dependent launches).  If capture is not possible here, the
+    # step is timed as eager launches instead; config.launch says which.
+    graph = None
+    if not args.no_graph:
+        try:
+            g_ = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_):
+                step(st=torch.cuda.current_stream())
+            torch.cuda.synchronize()
+            for _ in range(2):
+                l2_flush()
+                g_.replay()
+            torch.cuda.synchronize()
+            if nea.check_status(stream) != nea.NEA_OK:
+                raise RuntimeError("status word set by a graph replay")
+            graph = g_
+        except Exception as exc:  # noqa: BLE001 - reported in the JSON line
+            graph = None
+            graph_error = f"{type(exc).__name__}: {exc}"[:200]
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    gev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     barrier(ws)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         t0 = time.perf_counter()
         for i in range(K):
             l2_flush()
-            step(evs[i])
+            if graph is not None:
+                gev[i][0].record(stream)
+                graph.replay()
+                gev[i][1].record(stream)
+            else:
+                step(evs[i])
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
     barrier(ws)
     if nea.check_status(stream) != nea.NEA_OK:
         raise RuntimeError("kernel status word set during the timed region")
+    # per-kernel times: from the graph-less step (events between the kernels)
+    if graph is not None:
+        for i in range(K):
+            l2_flush()
+            step(evs[i])
+        torch.cuda.synchronize()
+        if nea.check_status(stream) != nea.NEA_OK:
+            raise RuntimeError("kernel status word set during the per-kernel timing")
     per = [[evs[i][s].elapsed_time(evs[i][s + 1]) for s in range(4)] for i in range(K)]
     # per[i] = [fwd, bwd_pre, bwd_main, bwd_post] in ms
-    step_ms = [sum(p) for p in per]
+    eager_ms = sum(sum(p) for p in per) / K
+    if graph is not None:
+        step_ms = [gev[i][0].elapsed_time(gev[i][1]) for i in range(K)]
+    else:
+        step_ms = [sum(p) for p in per]
     ms_step = max_over_ranks(sum(step_ms) / K, ws)
     flops = w.fwd_flops() + w.bwd_flops()
     value = job_value(flops, ms_step, ws)
@@ -362,6 +402,10 @@ def run_cuda(args):
                 "ms_per_step": round(e_ms_step, 4), "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo},
         "gpu_launches": 4 * K,
+        "launch": ("CUDA graph of the step's 4 kernels (replayed per step)" if graph is not None
+                   else "eager launches" + (f" (graph capture failed: {graph_error})"
+                                            if not args.no_graph else "")),
+        "eager_ms_per_step": round(eager_ms, 5),
         "clocks": clk.summary(),
         "wall_s_timed_region": round(wall, 4),
     }
@@ -527,6 +571,8 @@ def main():
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time the step as eager launches instead of a CUDA graph replay")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the RoPE and decode measurements")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(

@@ -3,9 +3,15 @@
 // "NanoEuler: Hand-writing GPT-2 in Pure C/CUDA", section "Tiled
 // FlashAttention": one block per query tile, an outer loop over key/value
 // tiles staged in shared memory, S = Q K^T, an online softmax update, and an
-// accumulated output.  Here, per CTA = one (batch, head, 128-row query tile):
+// accumulated output.  Here a work item is one (batch, head, 128-row query
+// tile).  bf16 CTAs are persistent: each walks a list of items (two CTAs per
+// SM at d = 64), loading the next item's Q and first K/V tiles and issuing
+// its first S = Q K^T while the current item's last tile and output are
+// still being finished, so that neither the load latency nor the output
+// store is paid once per item.  (tf32 has no shared memory left for a
+// separate output buffer and runs one item per CTA.)  Roles:
 //
-//   warp 0      TMA producer: Q once, then K_j / V_j into a 2-stage ring
+//   warp 0      TMA producer: per item Q, then K_j / V_j into a 2-stage ring
 //   warp 1      MMA issuer (one thread): S = Q K_j^T (SS), O += P V_j (TS,
 //               P read from tensor memory); owns the TMEM allocation
 //   warps 2..5  softmax: thread = query row (TMEM lane); reads S with
@@ -13,6 +19,9 @@
 //               sum in the log2 domain, writes P (bf16 or tf32) back to TMEM,
 //               rescales O only when the running max grew by more than 2^8;
 //               epilogue O / l -> smem -> TMA store, LSE -> global
+//
+// Every ring stage, barrier phase and TMEM hand-off counts tiles globally
+// over the CTA's items, so the pipeline runs on across item boundaries.
 //
 // Tensor memory (fp32 columns, lane = query row): S [0,128), O [128,128+d),
 // P [128+d, ...).  Key tiles above the causal diagonal are never loaded.
@@ -47,17 +56,47 @@ struct FwdCfg {
   static constexpr int THREADS = TRANSPOSE_V ? 320 : 192;
   static constexpr int VT_BYTES = TRANSPOSE_V ? TILE_BYTES : 0;
   static constexpr int VT_BLK_BYTES = D * 128;  // one 32-key column block of V^T
-  // Q tile, then per stage: K tile, V tile (, V^T).  +1 KB for alignment.
-  static constexpr int SMEM_BYTES = 1024 + TILE_BYTES * (1 + 2 * STAGES) + VT_BYTES * STAGES;
+  static_assert(STAGES >= 2, "S_{j+1} is issued before O += P_j V_j");
+  // Persistent CTAs stage O in a buffer of its own (Q's buffer takes the next
+  // item's Q); tf32 stages it in Q's buffer and runs one item per CTA.
+  static constexpr bool PERSIST = !TRANSPOSE_V;
+  static constexpr int O_BYTES = PERSIST ? TILE_BYTES : 0;
+  // Q tile, per stage: K tile, V tile (, V^T), then O.  +1 KB for alignment.
+  static constexpr int SMEM_BYTES =
+      1024 + TILE_BYTES * (1 + 2 * STAGES) + VT_BYTES * STAGES + O_BYTES;
 };
+
+// One work item: a query tile of one (batch, head).
+struct FwdItem {
+  int qt, bh, nkv;
+};
+
+// Item k of this CTA.  Items are ordered longest first (the causal diagonal
+// makes query tile qt cost qt + 1 key tiles) and dealt to the CTAs in a
+// zig-zag (k even: CTA c takes c of the k-th round, k odd: G-1-c), which
+// evens out the total work per CTA.
+__device__ __forceinline__ bool fwd_item(const FwdArgs& a, int T, int k, FwdItem& it) {
+  const long long G = gridDim.x, c = blockIdx.x;
+  const long long BH = static_cast<long long>(a.B) * a.H;
+  const long long idx = k * G + ((k & 1) ? (G - 1 - c) : c);
+  if (idx >= BH * T) return false;
+  it.qt = a.causal ? static_cast<int>(T - 1 - idx / BH) : static_cast<int>(idx / BH);
+  it.bh = static_cast<int>(idx % BH);
+  it.nkv = a.causal ? it.qt + 1 : T;
+  return true;
+}
 
 // mbarrier slots
 // P and O += P V are split in two halves of the key tile (keys 0..63 and
 // 64..127): PFULL1/ODONE1 and PFULL2/ODONE2, so that the first half's MMAs
 // run while the softmax computes the second half.
+// QEMPTY: the item's S MMAs are done, Q's buffer may take the next item's Q.
+// OFREE: the epilogue has read O from TMEM, the next item's P V may overwrite it.
 enum : int { B_QFULL = 0, B_SFULL, B_SFREE, B_PFULL1, B_PFULL2, B_ODONE1, B_ODONE2, B_DRAIN,
-             B_QREADY, B_KFULL };
-// K_FULL[s] = B_KFULL + s, V_FULL[s] = B_KFULL + ST + s, KV_EMPTY[s] = B_KFULL + 2 ST + s
+             B_QREADY, B_QEMPTY, B_OFREE, B_KFULL };
+// K_FULL[s] = B_KFULL + s, V_FULL[s] = B_KFULL + ST + s, V_EMPTY[s] = B_KFULL + 2 ST + s,
+// K_EMPTY[s] = B_KFULL + 5 ST + s.  K and V stages are freed separately: K_j
+// once S_j is done, V_j once P_j V_j is done.
 
 constexpr float kLog2e = 1.4426950408889634f;
 // Lazy rescale: O and l keep a stale row max until the true max exceeds it
@@ -73,23 +112,24 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   // + VT_FULL[s] = B_KFULL + 3 ST + s, KREADY[s] = B_KFULL + 4 ST + s (tf32)
-  __shared__ __align__(8) uint64_t bars[B_KFULL + 5 * ST];
+  __shared__ __align__(8) uint64_t bars[B_KFULL + 6 * ST];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = (a.N + kTile - 1) / kTile;  // the last tile may be partial
-  const int BH = a.B * a.H;
-  const int lin = blockIdx.x;
-  const int qt = a.causal ? (T - 1 - lin / BH) : (lin / BH);  // longest rows first
-  const int bh = lin % BH;
-  const int b = bh / a.H, h = bh % a.H;
-  const int kvh = b * a.Hkv + h / (a.H / a.Hkv);
-  const int nkv = a.causal ? qt + 1 : T;
+  FwdItem first;
+  if (!fwd_item(a, T, 0, first)) return;  // (the launcher makes no such CTA)
+  constexpr int kMaxItems = C::PERSIST ? 0x7fffffff : 1;  // items per CTA
+  auto kv_head = [&](const FwdItem& it) {
+    const int b = it.bh / a.H, h = it.bh % a.H;
+    return b * a.Hkv + h / (a.H / a.Hkv);
+  };
 
   const uint32_t sQ = smem_u32(smem);
   const uint32_t sKV = sQ + C::TILE_BYTES;  // stage s: K at +2s*TILE, V at +(2s+1)*TILE
   const uint32_t sVT = sKV + 2 * ST * C::TILE_BYTES;  // stage s: V^T at +s*VT_BYTES
+  const uint32_t sO = C::PERSIST ? sVT + ST * C::VT_BYTES : sQ;  // output staging
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   volatile int* abort = &abort_sh;
   unsigned int* status = a.status;
@@ -104,8 +144,11 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
     mbar_init(bar(B_ODONE1), 1);
     mbar_init(bar(B_ODONE2), 1);
     mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(B_QEMPTY), 1);
+    mbar_init(bar(B_OFREE), 128);
     for (int s = 0; s < 3 * ST; ++s) mbar_init(bar(B_KFULL + s), 1);
     for (int s = 0; s < 2 * ST; ++s) mbar_init(bar(B_KFULL + 3 * ST + s), 128);
+    for (int s = 0; s < ST; ++s) mbar_init(bar(B_KFULL + 5 * ST + s), 1);
     mbar_init(bar(B_QREADY), 128);
     fence_barrier_init();
   }
@@ -127,34 +170,80 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int issued = 0;
-      bool ok = true;
-      mbar_expect_tx(bar(B_QFULL), C::TILE_BYTES);
-      for (int k = 0; k < C::NBLK; ++k)
-        tma_load_3d(sQ + k * C::BLK_BYTES, &a.tmQ, bar(B_QFULL), k * C::BLK_ELEMS, qt * kTile, bh);
-      for (int j = 0; j < nkv; ++j) {
-        const int s = j % ST;
-        if (j >= ST && !mbar_wait(bar(B_KFULL + 2 * ST + s), ((j / ST) - 1) & 1, abort, 1, status)) {
-          ok = false;
-          break;
+      // K runs one tile ahead of V: K_g is read by S_g, which is issued
+      // before O += P_{g-1} V_{g-1}; V_g only by P_g V_g.  A stage of K is
+      // refilled once the S that read it is done, a stage of V once its P V
+      // is done.  An item's Q goes out just before its first K.
+      struct Cursor {
+        int k, j;
+        FwdItem it;
+        bool valid;
+      };
+      auto advance = [&](Cursor& cu) {
+        if (++cu.j == cu.it.nkv) {
+          ++cu.k;
+          cu.j = 0;
+          cu.valid = cu.k < kMaxItems && fwd_item(a, T, cu.k, cu.it);
         }
-        const uint32_t sK = sKV + (2 * s) * C::TILE_BYTES, sV = sK + C::TILE_BYTES;
-        mbar_expect_tx(bar(B_KFULL + s), C::TILE_BYTES);
-        for (int k = 0; k < C::NBLK; ++k)
-          tma_load_3d(sK + k * C::BLK_BYTES, &a.tmK, bar(B_KFULL + s), k * C::BLK_ELEMS,
-                      j * kTile, kvh);
-        mbar_expect_tx(bar(B_KFULL + ST + s), C::TILE_BYTES);
-        for (int k = 0; k < C::NBLK; ++k)
-          tma_load_3d(sV + k * C::BLK_BYTES, &a.tmV, bar(B_KFULL + ST + s), k * C::BLK_ELEMS,
-                      j * kTile, kvh);
-        issued = j + 1;
+      };
+      Cursor ck{0, 0, first, true}, cv{0, 0, first, true};
+      int gk = 0, gv = 0, qloads = 0;  // global tile index of the next K / V load
+      bool ok = true;
+      // One load per pass: K_0 K_1 V_0 K_2 V_1 ...; before a K that starts a
+      // new item (and so first waits for the previous item's S), the V loads
+      // still owed go out, so that they do not queue behind that wait.
+      while (ok && (ck.valid || cv.valid)) {
+        const bool v_due =
+            cv.valid && (!ck.valid || gv < gk - 1 || (gv < gk && ck.j == 0 && ck.k > 0));
+        if (!v_due) {
+          if (ck.j == 0) {
+            // Q's buffer is free once the previous item's S MMAs are done.
+            if (ck.k > 0 && !mbar_wait(bar(B_QEMPTY), (ck.k - 1) & 1, abort, 15, status)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(bar(B_QFULL), C::TILE_BYTES);
+            for (int kb = 0; kb < C::NBLK; ++kb)
+              tma_load_3d(sQ + kb * C::BLK_BYTES, &a.tmQ, bar(B_QFULL), kb * C::BLK_ELEMS,
+                          ck.it.qt * kTile, ck.it.bh);
+            qloads = ck.k + 1;
+          }
+          const int s = gk % ST;
+          if (gk >= ST &&
+              !mbar_wait(bar(B_KFULL + 5 * ST + s), ((gk / ST) - 1) & 1, abort, 1, status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sK = sKV + (2 * s) * C::TILE_BYTES;
+          mbar_expect_tx(bar(B_KFULL + s), C::TILE_BYTES);
+          for (int kb = 0; kb < C::NBLK; ++kb)
+            tma_load_3d(sK + kb * C::BLK_BYTES, &a.tmK, bar(B_KFULL + s), kb * C::BLK_ELEMS,
+                        ck.j * kTile, kv_head(ck.it));
+          ++gk;
+          advance(ck);
+        } else {
+          const int s = gv % ST;
+          if (gv >= ST &&
+              !mbar_wait(bar(B_KFULL + 2 * ST + s), ((gv / ST) - 1) & 1, abort, 17, status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sV = sKV + (2 * s + 1) * C::TILE_BYTES;
+          mbar_expect_tx(bar(B_KFULL + ST + s), C::TILE_BYTES);
+          for (int kb = 0; kb < C::NBLK; ++kb)
+            tma_load_3d(sV + kb * C::BLK_BYTES, &a.tmV, bar(B_KFULL + ST + s), kb * C::BLK_ELEMS,
+                        cv.j * kTile, kv_head(cv.it));
+          ++gv;
+          advance(cv);
+        }
       }
       if (!ok) {  // let the loads already issued land before the CTA exits
-        mbar_wait_drain(bar(B_QFULL), 0, 2, status);
-        for (int j = issued - ST > 0 ? issued - ST : 0; j < issued; ++j) {
-          mbar_wait_drain(bar(B_KFULL + j % ST), (j / ST) & 1, 2, status);
-          mbar_wait_drain(bar(B_KFULL + ST + j % ST), (j / ST) & 1, 2, status);
-        }
+        // (every earlier Q and tile was waited for by the MMA thread)
+        if (qloads > 0) mbar_wait_drain(bar(B_QFULL), (qloads - 1) & 1, 2, status);
+        for (int t = gk - ST > 0 ? gk - ST : 0; t < gk; ++t)
+          mbar_wait_drain(bar(B_KFULL + t % ST), (t / ST) & 1, 2, status);
+        for (int t = gv - ST > 0 ? gv - ST : 0; t < gv; ++t)
+          mbar_wait_drain(bar(B_KFULL + ST + t % ST), (t / ST) & 1, 2, status);
       }
     }
   } else if (warp == 1) {
@@ -162,60 +251,101 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
     if (lane == 0) {
       constexpr uint32_t idS = make_idesc<KIND>(128, 128, false, false);
       constexpr uint32_t idPV = make_idesc<KIND>(128, D, false, !C::TRANSPOSE_V);
-      auto issue_s = [&](int j) -> bool {
-        const int s = j % ST;
+      const int qbar = C::TRANSPOSE_V ? B_QREADY : B_QFULL;
+      // S for global tile g = tile j of item `it`.  After an item's last S,
+      // QEMPTY hands Q's buffer back to the producer.
+      auto issue_s = [&](int g, const FwdItem& it, int j) -> bool {
+        const int s = g % ST;
         const int kbar = C::TRANSPOSE_V ? B_KFULL + 4 * ST + s : B_KFULL + s;
-        if (!mbar_wait(bar(kbar), (j / ST) & 1, abort, 3, status)) return false;
+        if (!mbar_wait(bar(kbar), (g / ST) & 1, abort, 3, status)) return false;
         tc_fence_after();
         const uint32_t sK = sKV + (2 * s) * C::TILE_BYTES;
 #pragma unroll
-        for (int k = 0; k < C::NK_QK; ++k) {
-          const uint32_t off = ((k * 32) / 128) * C::BLK_BYTES + (k * 32) % 128;
+        for (int kk = 0; kk < C::NK_QK; ++kk) {
+          const uint32_t off = ((kk * 32) / 128) * C::BLK_BYTES + (kk * 32) % 128;
           mma_ss<KIND>(tmem + C::S_COL, sdesc_sw128(sQ + off, 16, 1024),
-                       sdesc_sw128(sK + off, 16, 1024), idS, k > 0 ? 1u : 0u);
+                       sdesc_sw128(sK + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(B_SFULL));
+        mma_commit(bar(B_KFULL + 5 * ST + s));  // K stage free for the producer
+        if (j == it.nkv - 1) mma_commit(bar(B_QEMPTY));
         return true;
       };
-      bool ok = mbar_wait(bar(C::TRANSPOSE_V ? B_QREADY : B_QFULL), 0, abort, 4, status) &&
-                issue_s(0);
-      for (int j = 0; ok && j < nkv; ++j) {
-        // S_{j+1} overwrites S once the softmax has read S_j.  With a ring of
-        // two stages it is issued before O += P_j V_j; with one stage K_{j+1}
-        // can only land after P_j V_j has freed the stage, so it goes after.
-        if (ST >= 2 && j + 1 < nkv) {
-          if (!mbar_wait(bar(B_SFREE), j & 1, abort, 5, status) || !issue_s(j + 1)) break;
-        }
-        const int s = j % ST;
-        const int vbar = C::TRANSPOSE_V ? B_KFULL + 3 * ST + s : B_KFULL + ST + s;
-        if (!mbar_wait(bar(vbar), (j / ST) & 1, abort, 7, status)) break;
-        const uint32_t sV = sKV + (2 * s + 1) * C::TILE_BYTES;
-        bool half_ok = true;
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          if (!mbar_wait(bar(hf == 0 ? B_PFULL1 : B_PFULL2), j & 1, abort, 6, status)) {
-            half_ok = false;
+      FwdItem cur = first;
+      int k = 0, g = 0;
+      bool ok = mbar_wait(bar(qbar), 0, abort, 4, status) && issue_s(0, cur, 0);
+      while (ok) {
+        FwdItem nx;
+        const bool has_next = k + 1 < kMaxItems && fwd_item(a, T, k + 1, nx);
+        for (int j = 0; j < cur.nkv; ++j, ++g) {
+          // S_{g+1} overwrites S once the softmax has read S_g; it is issued
+          // before O += P_g V_g.  At an item's last tile, the next item's
+          // first S goes first only if its Q has already landed; otherwise
+          // after this tile's P V, so that the Q load does not hold it up.
+          bool s_late = false;
+          if (j + 1 < cur.nkv || has_next) {
+            if (!mbar_wait(bar(B_SFREE), g & 1, abort, 5, status)) {
+              ok = false;
+              break;
+            }
+            if (j + 1 < cur.nkv) {
+              if (!issue_s(g + 1, cur, j + 1)) {
+                ok = false;
+                break;
+              }
+            } else if (mbar_test(bar(qbar), (k + 1) & 1)) {
+              if (!issue_s(g + 1, nx, 0)) {
+                ok = false;
+                break;
+              }
+            } else {
+              s_late = true;
+            }
+          }
+          // The item's first P V overwrites O: the previous epilogue must
+          // have read it.
+          if (j == 0 && k > 0 && !mbar_wait(bar(B_OFREE), (k - 1) & 1, abort, 16, status)) {
+            ok = false;
             break;
           }
-          tc_fence_after();
-#pragma unroll
-          for (int k = hf * C::NK_PV / 2; k < (hf + 1) * C::NK_PV / 2; ++k) {
-            uint64_t bdesc;
-            if constexpr (C::TRANSPOSE_V)  // V^T K-major: 32-B K-step, 4 per 128-B block
-              bdesc = sdesc_sw128(sVT + s * C::VT_BYTES + (k / 4) * C::VT_BLK_BYTES + (k % 4) * 32,
-                                  16, 1024);
-            else  // V MN-major: K-step = KPER rows of 128 B
-              bdesc = sdesc_sw128(sV + k * C::KPER * 128, C::BLK_BYTES, 1024);
-            mma_ts<KIND>(tmem + C::O_COL, tmem + C::P_COL + k * 8, bdesc, idPV,
-                         (j > 0 || k > 0) ? 1u : 0u);
+          const int s = g % ST;
+          const int vbar = C::TRANSPOSE_V ? B_KFULL + 3 * ST + s : B_KFULL + ST + s;
+          if (!mbar_wait(bar(vbar), (g / ST) & 1, abort, 7, status)) {
+            ok = false;
+            break;
           }
-          if (hf == 1) mma_commit(bar(B_KFULL + 2 * ST + s));  // stage s free for the producer
-          mma_commit(bar(hf == 0 ? B_ODONE1 : B_ODONE2));
+          const uint32_t sV = sKV + (2 * s + 1) * C::TILE_BYTES;
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            if (!mbar_wait(bar(hf == 0 ? B_PFULL1 : B_PFULL2), g & 1, abort, 6, status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = hf * C::NK_PV / 2; kk < (hf + 1) * C::NK_PV / 2; ++kk) {
+              uint64_t bdesc;
+              if constexpr (C::TRANSPOSE_V)  // V^T K-major: 32-B K-step, 4 per 128-B block
+                bdesc = sdesc_sw128(
+                    sVT + s * C::VT_BYTES + (kk / 4) * C::VT_BLK_BYTES + (kk % 4) * 32, 16, 1024);
+              else  // V MN-major: K-step = KPER rows of 128 B
+                bdesc = sdesc_sw128(sV + kk * C::KPER * 128, C::BLK_BYTES, 1024);
+              mma_ts<KIND>(tmem + C::O_COL, tmem + C::P_COL + kk * 8, bdesc, idPV,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            if (hf == 1) mma_commit(bar(B_KFULL + 2 * ST + s));  // V stage free for the producer
+            mma_commit(bar(hf == 0 ? B_ODONE1 : B_ODONE2));
+          }
+          if (!ok) break;
+          if (s_late && (!mbar_wait(bar(qbar), (k + 1) & 1, abort, 4, status) ||
+                         !issue_s(g + 1, nx, 0))) {
+            ok = false;
+            break;
+          }
         }
-        if (!half_ok) break;
-        if (ST == 1 && j + 1 < nkv) {
-          if (!mbar_wait(bar(B_SFREE), j & 1, abort, 5, status) || !issue_s(j + 1)) break;
-        }
+        if (!ok || !has_next) break;
+        cur = nx;
+        ++k;
       }
       // Everything this thread issued must finish before TMEM is freed.
       mma_commit(bar(B_DRAIN));
@@ -243,16 +373,26 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
         }
         fence_proxy_async();
       };
-      if (mbar_wait_warp(bar(B_QFULL), 0, abort, 13, status)) {
+      int g = 0;
+      bool ok = true;
+      FwdItem it;
+      for (int k = 0; ok && k < kMaxItems && fwd_item(a, T, k, it); ++k) {
+        if (!mbar_wait_warp(bar(B_QFULL), k & 1, abort, 13, status)) break;
         round_tile(sQ);
         mbar_arrive(bar(B_QREADY));
-        for (int j = 0; j < nkv; ++j) {
-          const int s = j % ST;
-          const uint32_t ph = (j / ST) & 1;
-          if (!mbar_wait_warp(bar(B_KFULL + s), ph, abort, 14, status)) break;
+        for (int j = 0; j < it.nkv; ++j, ++g) {
+          const int s = g % ST;
+          const uint32_t ph = (g / ST) & 1;
+          if (!mbar_wait_warp(bar(B_KFULL + s), ph, abort, 14, status)) {
+            ok = false;
+            break;
+          }
           round_tile(sKV + (2 * s) * C::TILE_BYTES);
           mbar_arrive(bar(B_KFULL + 4 * ST + s));
-          if (!mbar_wait_warp(bar(B_KFULL + ST + s), ph, abort, 12, status)) break;
+          if (!mbar_wait_warp(bar(B_KFULL + ST + s), ph, abort, 12, status)) {
+            ok = false;
+            break;
+          }
           const uint8_t* vrow = smem + (sKV - sQ) + (2 * s + 1) * C::TILE_BYTES + t * 128;
           uint8_t* vt =
               smem + (sVT - sQ) + s * C::VT_BYTES + (t / 32) * C::VT_BLK_BYTES + (t % 4) * 4;
@@ -283,178 +423,192 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
     const int r = quad * 32 + lane;  // row of the query tile == TMEM lane
     const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const float c = a.scale * kLog2e;
-    float m_ref = -INFINITY, l = 0.f;
+    // On an abort the warps keep walking the item list without waiting, so
+    // that all four take part in the same named-barrier syncs.
     bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      if (!mbar_wait_warp(bar(B_SFULL), j & 1, abort, 9, status)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t u0[32], u1[32], u2[32], u3[32];
-      tmem_ld32(trow + C::S_COL + 0, u0);
-      tmem_ld32(trow + C::S_COL + 32, u1);
-      tmem_ld32(trow + C::S_COL + 64, u2);
-      tmem_ld32(trow + C::S_COL + 96, u3);
-      tmem_ld_wait(u0);
-      reg_fence(u1);
-      reg_fence(u2);
-      reg_fence(u3);
-      tc_fence_before();
-      mbar_arrive(bar(B_SFREE));
-      float sv[128];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        sv[i] = __uint_as_float(u0[i]);
-        sv[32 + i] = __uint_as_float(u1[i]);
-        sv[64 + i] = __uint_as_float(u2[i]);
-        sv[96 + i] = __uint_as_float(u3[i]);
-      }
-      // Keys past `lim` are masked: above the diagonal on the diagonal tile
-      // (which also covers keys past N under the causal mask: a padded key
-      // lies after every real query), and keys past N on the last tile
-      // otherwise.  TMA fills rows past N with zeros.
-      int lim = kTile - 1;
-      if (a.causal && j == qt) lim = r;
-      else if (!a.causal && j == T - 1) lim = a.N - 1 - j * kTile;
-      if (lim < kTile - 1) {
-#pragma unroll
-        for (int i = 0; i < 128; ++i)
-          if (i > lim) sv[i] = -INFINITY;
-      }
-      // row max as a tree (8 independent chains), not a 128-long chain
-      float mv[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mv[k] = sv[k];
-#pragma unroll
-      for (int i = 8; i < 128; i += 8) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mv[k] = fmaxf(mv[k], sv[i + k]);
-      }
-      const float mx = fmaxf(fmaxf(fmaxf(mv[0], mv[1]), fmaxf(mv[2], mv[3])),
-                             fmaxf(fmaxf(mv[4], mv[5]), fmaxf(mv[6], mv[7])));
-      const float m_new = fmaxf(m_ref, mx);
-      const bool need = (m_new - m_ref) * c > kRescaleLog2;  // always true on the first tile
-      float alpha = 1.f;
-      if (need) {
-        alpha = ex2((m_ref - m_new) * c);
-        m_ref = m_new;
-      }
-      const float moff = -m_ref * c;
-      // exponent arguments with packed fp32x2 FMAs; row sum in 4 packed chains
-      const float2 c2 = make_float2(c, c), moff2 = make_float2(moff, moff);
-      float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                       make_float2(0.f, 0.f)};
-      // Two halves of the key tile.  Half h of P may be overwritten once the
-      // half-h MMAs of tile j-1 are done (ODONE_h); O is rescaled only after
-      // both halves of tile j-1 are done and before PFULL1 releases tile j.
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        if (j > 0) {
-          if (!mbar_wait_warp(bar(hf == 0 ? B_ODONE1 : B_ODONE2), (j - 1) & 1, abort, 10,
-                              status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+    int g = 0;  // global tile index
+    FwdItem it;
+    for (int k = 0; k < kMaxItems && fwd_item(a, T, k, it); ++k) {
+      float m_ref = -INFINITY, l = 0.f;
+      for (int j = 0; ok && j < it.nkv; ++j, ++g) {
+        if (!mbar_wait_warp(bar(B_SFULL), g & 1, abort, 9, status)) {
+          ok = false;
+          break;
         }
-#pragma unroll
-        for (int cc = 2 * hf; cc < 2 * hf + 2; ++cc) {
-          float p[32];
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const float2 x =
-                __ffma2_rn(make_float2(sv[32 * cc + i], sv[32 * cc + i + 1]), c2, moff2);
-            p[i] = ex2(x.x);
-            p[i + 1] = ex2(x.y);
-            rs2[(i >> 1) & 3] = __fadd2_rn(rs2[(i >> 1) & 3], make_float2(p[i], p[i + 1]));
-          }
-          if constexpr (KIND == MmaKind::kBF16) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(p[2 * i], p[2 * i + 1]);
-            tmem_st16(trow + C::P_COL + 16 * cc, pk);
-          } else {
-            uint32_t pk[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) pk[i] = __float_as_uint(p[i]);
-            tmem_st32(trow + C::P_COL + 32 * cc, pk);
-          }
-        }
-        if (hf == 0 && j > 0 && __any_sync(0xffffffffu, need)) {
-          // O rescale: needs the half-2 MMAs of tile j-1 done as well
-          if (!mbar_wait_warp(bar(B_ODONE2), (j - 1) & 1, abort, 10, status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll
-          for (int cc = 0; cc < D; cc += 32) {
-            uint32_t o[32];
-            tmem_ld32(trow + C::O_COL + cc, o);
-            tmem_ld_wait(o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(trow + C::O_COL + cc, o);
-          }
-        }
-        tmem_st_wait();
+        tc_fence_after();
+        uint32_t u0[32], u1[32], u2[32], u3[32];
+        tmem_ld32(trow + C::S_COL + 0, u0);
+        tmem_ld32(trow + C::S_COL + 32, u1);
+        tmem_ld32(trow + C::S_COL + 64, u2);
+        tmem_ld32(trow + C::S_COL + 96, u3);
+        tmem_ld_wait(u0);
+        reg_fence(u1);
+        reg_fence(u2);
+        reg_fence(u3);
         tc_fence_before();
-        mbar_arrive(bar(hf == 0 ? B_PFULL1 : B_PFULL2));
-      }
-      if (!ok) break;
-      const float2 r01 = __fadd2_rn(rs2[0], rs2[1]), r23 = __fadd2_rn(rs2[2], rs2[3]);
-      const float rs = (r01.x + r01.y) + (r23.x + r23.y);
-      l = l * alpha + rs;
-    }
-    // ------------------------------------------------------------ epilogue
-    if (ok) ok = mbar_wait_warp(bar(B_ODONE2), (nkv - 1) & 1, abort, 11, status);
-    if (ok) {
-      tc_fence_after();
-      const float inv = 1.f / l;
-      uint8_t* orow = smem + r * 128;  // Q's smem is free: every MMA is done
+        mbar_arrive(bar(B_SFREE));
+        float sv[128];
 #pragma unroll
-      for (int cc = 0; cc < D; cc += 32) {
-        uint32_t o[32];
-        tmem_ld32(trow + C::O_COL + cc, o);
-        tmem_ld_wait(o);
-        if constexpr (KIND == MmaKind::kBF16) {
+        for (int i = 0; i < 32; ++i) {
+          sv[i] = __uint_as_float(u0[i]);
+          sv[32 + i] = __uint_as_float(u1[i]);
+          sv[64 + i] = __uint_as_float(u2[i]);
+          sv[96 + i] = __uint_as_float(u3[i]);
+        }
+        // Keys past `lim` are masked: above the diagonal on the diagonal tile
+        // (which also covers keys past N under the causal mask: a padded key
+        // lies after every real query), and keys past N on the last tile
+        // otherwise.  TMA fills rows past N with zeros.
+        int lim = kTile - 1;
+        if (a.causal && j == it.qt) lim = r;
+        else if (!a.causal && j == T - 1) lim = a.N - 1 - j * kTile;
+        if (lim < kTile - 1) {
 #pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {  // 4 chunks of 8 bf16 = 16 B
-            const int col = cc + 8 * q8;
-            const int blk = col / C::BLK_ELEMS, chunk = (col % C::BLK_ELEMS) / 8;
-            uint4 v;
-            v.x = pack_bf16(__uint_as_float(o[8 * q8 + 0]) * inv, __uint_as_float(o[8 * q8 + 1]) * inv);
-            v.y = pack_bf16(__uint_as_float(o[8 * q8 + 2]) * inv, __uint_as_float(o[8 * q8 + 3]) * inv);
-            v.z = pack_bf16(__uint_as_float(o[8 * q8 + 4]) * inv, __uint_as_float(o[8 * q8 + 5]) * inv);
-            v.w = pack_bf16(__uint_as_float(o[8 * q8 + 6]) * inv, __uint_as_float(o[8 * q8 + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + blk * C::BLK_BYTES + ((chunk ^ (r & 7)) << 4)) = v;
+          for (int i = 0; i < 128; ++i)
+            if (i > lim) sv[i] = -INFINITY;
+        }
+        // row max as a tree (8 independent chains), not a 128-long chain
+        float mv[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mv[k] = sv[k];
+#pragma unroll
+        for (int i = 8; i < 128; i += 8) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mv[k] = fmaxf(mv[k], sv[i + k]);
+        }
+        const float mx = fmaxf(fmaxf(fmaxf(mv[0], mv[1]), fmaxf(mv[2], mv[3])),
+                               fmaxf(fmaxf(mv[4], mv[5]), fmaxf(mv[6], mv[7])));
+        const float m_new = fmaxf(m_ref, mx);
+        const bool need = (m_new - m_ref) * c > kRescaleLog2;  // always true on the first tile
+        float alpha = 1.f;
+        if (need) {
+          alpha = ex2((m_ref - m_new) * c);
+          m_ref = m_new;
+        }
+        const float moff = -m_ref * c;
+        // exponent arguments with packed fp32x2 FMAs; row sum in 4 packed chains
+        const float2 c2 = make_float2(c, c), moff2 = make_float2(moff, moff);
+        float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
+        // Two halves of the key tile.  Half h of P may be overwritten once the
+        // half-h MMAs of the previous tile (of this or the previous item) are
+        // done (ODONE_h); O is rescaled only after both halves of tile j-1 are
+        // done and before PFULL1 releases tile j.
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          if (g > 0) {
+            if (!mbar_wait_warp(bar(hf == 0 ? B_ODONE1 : B_ODONE2), (g - 1) & 1, abort, 10,
+                                status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
           }
-        } else {
 #pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {  // 8 chunks of 4 fp32 = 16 B
-            const int col = cc + 4 * q4;
-            const int blk = col / C::BLK_ELEMS, chunk = (col % C::BLK_ELEMS) / 4;
-            uint4 v;
-            v.x = __float_as_uint(__uint_as_float(o[4 * q4 + 0]) * inv);
-            v.y = __float_as_uint(__uint_as_float(o[4 * q4 + 1]) * inv);
-            v.z = __float_as_uint(__uint_as_float(o[4 * q4 + 2]) * inv);
-            v.w = __float_as_uint(__uint_as_float(o[4 * q4 + 3]) * inv);
-            *reinterpret_cast<uint4*>(orow + blk * C::BLK_BYTES + ((chunk ^ (r & 7)) << 4)) = v;
+          for (int cc = 2 * hf; cc < 2 * hf + 2; ++cc) {
+            float p[32];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const float2 x =
+                  __ffma2_rn(make_float2(sv[32 * cc + i], sv[32 * cc + i + 1]), c2, moff2);
+              p[i] = ex2(x.x);
+              p[i + 1] = ex2(x.y);
+              rs2[(i >> 1) & 3] = __fadd2_rn(rs2[(i >> 1) & 3], make_float2(p[i], p[i + 1]));
+            }
+            if constexpr (KIND == MmaKind::kBF16) {
+              uint32_t pk[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(p[2 * i], p[2 * i + 1]);
+              tmem_st16(trow + C::P_COL + 16 * cc, pk);
+            } else {
+              uint32_t pk[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) pk[i] = __float_as_uint(p[i]);
+              tmem_st32(trow + C::P_COL + 32 * cc, pk);
+            }
+          }
+          if (hf == 0 && j > 0 && __any_sync(0xffffffffu, need)) {
+            // O rescale: needs the half-2 MMAs of tile j-1 done as well
+            if (!mbar_wait_warp(bar(B_ODONE2), (g - 1) & 1, abort, 10, status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int cc = 0; cc < D; cc += 32) {
+              uint32_t o[32];
+              tmem_ld32(trow + C::O_COL + cc, o);
+              tmem_ld_wait(o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st32(trow + C::O_COL + cc, o);
+            }
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bar(hf == 0 ? B_PFULL1 : B_PFULL2));
+        }
+        if (!ok) break;
+        const float2 r01 = __fadd2_rn(rs2[0], rs2[1]), r23 = __fadd2_rn(rs2[2], rs2[3]);
+        const float rs = (r01.x + r01.y) + (r23.x + r23.y);
+        l = l * alpha + rs;
+      }
+      // ------------------------------------------------------------ epilogue
+      if (ok) ok = mbar_wait_warp(bar(B_ODONE2), (g - 1) & 1, abort, 11, status);
+      if (k > 0) {  // the previous item's store must have read the staging buffer
+        if (warp == 2 && lane == 0) bulk_wait_read0();
+        named_bar_sync(1, 128);
+      }
+      if (ok) {
+        tc_fence_after();
+        const float inv = 1.f / l;
+        // (tf32 stages O in Q's buffer: free, as every MMA of the CTA is done)
+        uint8_t* orow = smem + (sO - sQ) + r * 128;
+#pragma unroll
+        for (int cc = 0; cc < D; cc += 32) {
+          uint32_t o[32];
+          tmem_ld32(trow + C::O_COL + cc, o);
+          tmem_ld_wait(o);
+          if constexpr (KIND == MmaKind::kBF16) {
+#pragma unroll
+            for (int q8 = 0; q8 < 4; ++q8) {  // 4 chunks of 8 bf16 = 16 B
+              const int col = cc + 8 * q8;
+              const int blk = col / C::BLK_ELEMS, chunk = (col % C::BLK_ELEMS) / 8;
+              uint4 v;
+              v.x = pack_bf16(__uint_as_float(o[8 * q8 + 0]) * inv, __uint_as_float(o[8 * q8 + 1]) * inv);
+              v.y = pack_bf16(__uint_as_float(o[8 * q8 + 2]) * inv, __uint_as_float(o[8 * q8 + 3]) * inv);
+              v.z = pack_bf16(__uint_as_float(o[8 * q8 + 4]) * inv, __uint_as_float(o[8 * q8 + 5]) * inv);
+              v.w = pack_bf16(__uint_as_float(o[8 * q8 + 6]) * inv, __uint_as_float(o[8 * q8 + 7]) * inv);
+              *reinterpret_cast<uint4*>(orow + blk * C::BLK_BYTES + ((chunk ^ (r & 7)) << 4)) = v;
+            }
+          } else {
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {  // 8 chunks of 4 fp32 = 16 B
+              const int col = cc + 4 * q4;
+              const int blk = col / C::BLK_ELEMS, chunk = (col % C::BLK_ELEMS) / 4;
+              uint4 v;
+              v.x = __float_as_uint(__uint_as_float(o[4 * q4 + 0]) * inv);
+              v.y = __float_as_uint(__uint_as_float(o[4 * q4 + 1]) * inv);
+              v.z = __float_as_uint(__uint_as_float(o[4 * q4 + 2]) * inv);
+              v.w = __float_as_uint(__uint_as_float(o[4 * q4 + 3]) * inv);
+              *reinterpret_cast<uint4*>(orow + blk * C::BLK_BYTES + ((chunk ^ (r & 7)) << 4)) = v;
+            }
           }
         }
+        tc_fence_before();
+        mbar_arrive(bar(B_OFREE));  // O is in registers: the next item may overwrite it
+        if (it.qt * kTile + r < a.N)  // rows past N exist only in smem; TMA clips O
+          a.lse[static_cast<size_t>(it.bh) * a.N + it.qt * kTile + r] = m_ref * a.scale + logf(l);
+        fence_proxy_async();
       }
-      if (qt * kTile + r < a.N)  // rows past N exist only in smem; TMA clips O
-        a.lse[static_cast<size_t>(bh) * a.N + qt * kTile + r] = m_ref * a.scale + logf(l);
-      fence_proxy_async();
-    }
-    named_bar_sync(1, 128);
-    if (warp == 2 && lane == 0 && !*abort) {
-      for (int k = 0; k < C::NBLK; ++k)
-        tma_store_3d(&a.tmO, sQ + k * C::BLK_BYTES, k * C::BLK_ELEMS, qt * kTile, bh);
-      bulk_commit();
-      bulk_wait0();
-    }
+      named_bar_sync(1, 128);
+      if (warp == 2 && lane == 0 && !*abort) {
+        for (int kb = 0; kb < C::NBLK; ++kb)
+          tma_store_3d(&a.tmO, sO + kb * C::BLK_BYTES, kb * C::BLK_ELEMS, it.qt * kTile, it.bh);
+        bulk_commit();
+      }
+    }  // items
+    if (warp == 2 && lane == 0) bulk_wait0();
   }
   tc_fence_before();
   __syncthreads();
@@ -466,23 +620,26 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
 }
 
 template <int D, MmaKind KIND>
-cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
+cudaError_t launch_fwd_t(const FwdArgs& a, int sms, cudaStream_t stream) {
   using C = FwdCfg<D, KIND>;
   auto kern = fwd_kernel<D, KIND>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const unsigned grid = static_cast<unsigned>(a.B) * a.H * ((a.N + kTile - 1) / kTile);
+  const long long items = static_cast<long long>(a.B) * a.H * ((a.N + kTile - 1) / kTile);
+  // persistent: one wave of CTAs (no more CTAs than items: each gets one)
+  const long long slots = static_cast<long long>(sms > 0 ? sms : 1) * C::CTAS_PER_SM;
+  const unsigned grid = static_cast<unsigned>(C::PERSIST && slots < items ? slots : items);
   kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
-  if (a.dtype == 0 && a.d == 64) return launch_fwd_t<64, MmaKind::kBF16>(a, stream);
-  if (a.dtype == 0 && a.d == 128) return launch_fwd_t<128, MmaKind::kBF16>(a, stream);
-  if (a.dtype == 1 && a.d == 64) return launch_fwd_t<64, MmaKind::kTF32>(a, stream);
+cudaError_t launch_fwd(const FwdArgs& a, int sms, cudaStream_t stream) {
+  if (a.dtype == 0 && a.d == 64) return launch_fwd_t<64, MmaKind::kBF16>(a, sms, stream);
+  if (a.dtype == 0 && a.d == 128) return launch_fwd_t<128, MmaKind::kBF16>(a, sms, stream);
+  if (a.dtype == 1 && a.d == 64) return launch_fwd_t<64, MmaKind::kTF32>(a, sms, stream);
   return cudaErrorInvalidValue;
 }
 

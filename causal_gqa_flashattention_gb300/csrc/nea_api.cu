@@ -202,7 +202,9 @@ int nea_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LS
   if (!a.status) return NEA_ERR_CUDA;
   a.B = B; a.H = H; a.Hkv = Hkv; a.N = N; a.d = d; a.causal = causal;
   a.scale = scale; a.dtype = dtype;
-  return launch_fwd(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? NEA_OK : NEA_ERR_CUDA;
+  return launch_fwd(a, sm_count(), static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? NEA_OK
+             : NEA_ERR_CUDA;
 }
 
 size_t nea_attn_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d, int dtype) {

@@ -70,7 +70,8 @@ int decode_chunk_rows();
 
 // Each launcher validates nothing (the API layer did) and returns the
 // cudaError_t of its launch(es).
-cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
+// bf16: a persistent wave of min(items, sms x CTAs per SM) CTAs; tf32: one CTA per item.
+cudaError_t launch_fwd(const FwdArgs& a, int sms, cudaStream_t stream);
 cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_post(const BwdArgs& a, cudaStream_t stream);

@@ -126,6 +126,21 @@ def test_ragged_lengths(nea, w):
     run_case(nea, w)
 
 
+# The forward runs one wave of persistent CTAs (two per SM at d = 64, one at
+# d = 128 on a 152-SM GB300), each walking several (head, query tile) items:
+# more items than CTAs, with a partial last tile, causal and full masks.
+MULTI_ITEM = [
+    custom(4, 12, 4, 1000, 64),                 # 384 items, ragged, causal
+    custom(2, 12, 4, 1700, 64, causal=False),   # 336 items, ragged, full mask
+    custom(2, 8, 2, 1300, 128),                 # 176 items at d = 128
+]
+
+
+@pytest.mark.parametrize("w", MULTI_ITEM, ids=lambda w: w.name)
+def test_forward_items_per_cta(nea, w):
+    run_case(nea, w)
+
+
 def test_second_seed_and_repeat(nea):
     w = custom(1, 6, 2, 512, 64)
     run_case(nea, w, seed=1)

@@ -7,11 +7,14 @@
 // tile).  bf16 CTAs are persistent: each walks a list of items (two CTAs per
 // SM at d = 64), loading the next item's Q and first K/V tiles and issuing
 // its first S = Q K^T while the current item's last tile and output are
-// still being finished, so that neither the load latency nor the output
-// store is paid once per item.  (tf32 has no shared memory left for a
-// separate output buffer and runs one item per CTA.)  Roles:
+// still being finished, so that most of the load latency and the output
+// store overlap other work instead of being paid in full per item.  (tf32
+// has no shared memory left for a separate output buffer and runs one item
+// per CTA.)  Roles:
 //
-//   warp 0      TMA producer: per item Q, then K_j / V_j into a 2-stage ring
+//   warp 0      TMA producer: per item Q, then K_j and V_j into 2-stage
+//               rings, K one tile ahead of V (K_j is released after S_j,
+//               V_j after P_j V_j)
 //   warp 1      MMA issuer (one thread): S = Q K_j^T (SS), O += P V_j (TS,
 //               P read from tensor memory); owns the TMEM allocation
 //   warps 2..5  softmax: thread = query row (TMEM lane); reads S with

@@ -339,8 +339,10 @@ def run_cuda(args):
     def e2e_step(start=None):
         # dO is first needed by the backward: its copy runs on a side stream,
         # after the step's start event, while Q, K, V are copied and the
-        # forward runs; the backward waits for it.  (Spreading the other
-        # copies over more streams was slower: they share one link.)
+        # forward runs; the backward waits for it.  The backward runs as its
+        # three public stages so that dK and dV can go back to the host while
+        # dQ is cast; the step ends when every copy is done.  (Spreading the
+        # H2D copies over more streams was slower: they share one link.)
         if start is None:  # order the side stream after the previous step's work
             start = torch.cuda.Event()
             start.record(stream)
@@ -355,10 +357,28 @@ def run_cuda(args):
             o2, l2 = nea.attn_fwd(din[0], din[1], din[2], causal=True, scale=w.scale,
                                   stream=stream)
             stream.wait_event(do_ready)
-            nea.attn_bwd(din[0], din[1], din[2], o2, din[3], l2, causal=True, scale=w.scale,
-                         dq=dq2, dk=dk2, dv=dv2, workspace=wsp, stream=stream)
-            for h_, d_ in zip(hout, (dq2, dk2, dv2)):
-                h_.copy_(d_, non_blocking=True)
+
+            def after_stage(i):
+                # dK and dV are final once the main stage is done: they go
+                # back on the side stream while the dQ cast runs
+                if i == 2 and w.dtype == "bf16":
+                    kv_done = torch.cuda.Event()
+                    kv_done.record(stream)
+                    side.wait_event(kv_done)
+                    with torch.cuda.stream(side):
+                        hout[1].copy_(dk2, non_blocking=True)
+                        hout[2].copy_(dv2, non_blocking=True)
+
+            nea.attn_bwd_stages(din[0], din[1], din[2], o2, din[3], l2, dq2, dk2, dv2, wsp,
+                                causal=True, scale=w.scale, stream=stream, between=after_stage)
+            hout[0].copy_(dq2, non_blocking=True)
+            if w.dtype != "bf16":
+                hout[1].copy_(dk2, non_blocking=True)
+                hout[2].copy_(dv2, non_blocking=True)
+            else:
+                back = torch.cuda.Event()
+                back.record(side)
+                stream.wait_event(back)
 
     for _ in range(max(args.warmup, 3)):
         e2e_step()

@@ -62,9 +62,12 @@ typedef enum { NEA_BF16 = 0, NEA_F32 = 1 } nea_dtype;
 
 /*
  * Forward.  Writes O [B,H,N,d] (dtype) and LSE [B,H,N] (fp32, natural log).
- * Section "Tiled FlashAttention": one CTA per 128-row query tile of one
- * (batch, head); K/V tiles of 128 rows stream through shared memory; tiles
- * entirely above the causal diagonal are skipped.
+ * Section "Tiled FlashAttention": the work is one item per 128-row query tile
+ * of one (batch, head); K/V tiles of 128 rows stream through shared memory;
+ * tiles entirely above the causal diagonal are skipped.  bf16 runs one wave
+ * of persistent CTAs that each take several items; fp32 one CTA per item.
+ * One launch on `stream`; no allocation; returns NEA_OK or the error code of
+ * the first failed check or launch.
  */
 int nea_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
                  int Hkv, int N, int d, float scale, int causal, int dtype, void* stream);

@@ -72,14 +72,15 @@ def kernel_file_hash():
     return h.hexdigest()[:16]
 
 
-def traffic_for(kernel):
+def traffic_for(kernel, workload):
     """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernels have changed since the counters were taken."""
+    kernels have changed since the counters were taken or the counters were
+    taken on another workload (traffic depends on the shape)."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
-    if d.get("kernel_hash") != kernel_file_hash():
+    if d.get("kernel_hash") != kernel_file_hash() or d.get("workload_key") != workload:
         return None
     return d.get("per_launch_bytes", {}).get(kernel)
 
@@ -185,15 +186,68 @@ class ClockSampler:
 
 
 def dist_setup():
+    """Joins the process group when launched as one of several ranks: NCCL,
+    one GPU per rank, on a GPU machine; gloo where there is no GPU (host tests)."""
     import torch
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if ws > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("gloo")
     return ws, rank, local
+
+
+def _free_port():
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, n, port, target, args):
+    os.environ.update(RANK=str(rank), LOCAL_RANK=str(rank), WORLD_SIZE=str(n),
+                      LOCAL_WORLD_SIZE=str(n), MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    target(args)
+
+
+def spawn_local_ranks(n, target, args):
+    """Runs ``target(args)`` in n local processes, one per GPU, as ranks
+    0..n-1 of one job (the same environment torchrun gives each rank).
+    Returns the first non-zero exit code, or 0."""
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, n, port, target, args)) for r in range(n)]
+    for p in procs:
+        p.start()
+    rc = 0
+    for p in procs:
+        p.join()
+        if p.exitcode and not rc:
+            rc = p.exitcode
+    return rc
+
+
+def check_gpus(requested, world_size, visible):
+    """How --gpus is honoured: 'run' (this process is one of the job's ranks,
+    or the job has one GPU), 'spawn' (start that many local ranks), or an
+    error message."""
+    if requested < 1:
+        return "--gpus must be at least 1"
+    if world_size is not None:
+        if world_size != requested:
+            return f"--gpus {requested} but the launcher started {world_size} ranks"
+        return "run"
+    if requested == 1:
+        return "run"
+    if visible < requested:
+        return f"--gpus {requested} but only {visible} GPU(s) are visible"
+    return "spawn"
 
 
 def barrier(ws):
@@ -413,7 +467,7 @@ def run_cuda(args):
         "roofline": {"kernel": "bwd_main", "bound": "tensor", "achieved": round(main_tf, 1),
                      "peak": peak_tc, "unit": "TFLOP/s", "frac": round(main_tf / peak_tc, 4),
                      "peak_source": f"bf16_tflops (burst) of {src}",
-                     "traffic": traffic_for("bwd_main")},
+                     "traffic": traffic_for("bwd_main", w.name)},
         "kernels": {
             "fwd": {"ms": round(k_ms[0], 5),
                     "tflops": round(w.fwd_flops() / (k_ms[0] * 1e-3) / 1e12, 1)},
@@ -607,10 +661,19 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "cuda":
         args.warmup = 3
+    ws_env = os.environ.get("WORLD_SIZE")
     if args.impl == "reference":
+        # the oracle runs on the host cores of rank 0 only, whatever N is
         run_reference(args)
-    else:
-        run_cuda(args)
+        return
+    import torch
+    how = check_gpus(args.gpus, int(ws_env) if ws_env else None,
+                     torch.cuda.device_count() if torch.cuda.is_available() else 0)
+    if how == "spawn":
+        sys.exit(spawn_local_ranks(args.gpus, run_cuda, args))
+    if how != "run":
+        sys.exit(f"bench.py: {how}")
+    run_cuda(args)
 
 
 if __name__ == "__main__":

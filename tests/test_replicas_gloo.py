@@ -64,3 +64,33 @@ def test_reference_arm_other_ranks_exit_without_work(capsys, monkeypatch):
         steps, warmup = 1, 0
     bench.run_reference(Args())
     assert capsys.readouterr().out == ""
+
+
+def _spawned_rank(out_dir):
+    """Target of bench.spawn_local_ranks: joins the job the way run_cuda
+    does (gloo here, without a GPU), then records what it saw."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    import bench
+    ws, rank, local = bench.dist_setup()
+    try:
+        bench.barrier(ws)
+        worst = bench.max_over_ranks(0.1 + 0.01 * rank, ws)
+        with open(os.path.join(out_dir, f"rank{rank}.txt"), "w") as f:
+            f.write(f"{ws} {rank} {local} {worst:.6f}")
+    finally:
+        dist.destroy_process_group()
+
+
+def test_gpus_flag_spawns_local_ranks(tmp_path):
+    """bench.py --gpus N without torchrun starts N ranks itself; each gets
+    RANK / LOCAL_RANK / WORLD_SIZE as torchrun would set them and joins one
+    process group."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    rc = bench.spawn_local_ranks(2, _spawned_rank, str(tmp_path))
+    assert rc == 0
+    got = sorted((tmp_path / f"rank{r}.txt").read_text().split() for r in range(2))
+    assert got == [["2", "0", "0", "0.110000"], ["2", "1", "1", "0.110000"]]

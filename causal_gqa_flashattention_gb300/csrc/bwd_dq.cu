@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1) dq_bf16_kernel(const __g
     const float c = a.scale * kLog2e;
     const size_t row = static_cast<size_t>(bh) * a.N + static_cast<size_t>(it) * kTile + r;
     const size_t prow = (static_cast<size_t>(bh) * T + it) * kTile + r;  // padded per-row terms
-    const float l2 = a.lse2[prow], dsr = a.delta[prow];
+    const float nl2 = a.lse2[prow], dsr = a.delta[prow];
     const bool row_ok = it * kTile + r < a.N;
     bool ok = true;
     for (int jj = 0; jj < nkv; ++jj) {
@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1) dq_bf16_kernel(const __g
 #pragma unroll
       for (int t = 0; t < 64; ++t) {
         const float sv = __uint_as_float(t < 32 ? u0[t] : u1[t - 32]);
-        float pv = ex2(fmaf(sv, c, -l2));
+        float pv = ex2(fmaf(sv, c, nl2));
         if ((diag && k0 + t > r) || k0 + t > klim) pv = 0.f;
         p[t] = pv;
       }

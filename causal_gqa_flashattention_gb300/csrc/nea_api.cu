@@ -132,9 +132,10 @@ int check_common(int B, int H, int Hkv, int N, int d, float scale, int causal, i
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// bf16: D, L2, fp32 dQ accumulator.  fp32: D, L2, Q^T, dO^T, K^T (tf32).
+// bf16: D, -L2, fp32 dQ accumulator, row-term tiles.  fp32: D, -L2, Q^T,
+// dO^T, K^T (tf32).
 struct WsLayout {
-  size_t delta, lse2, dqacc, qt, dot, kt, total;
+  size_t delta, lse2, dqacc, fold, qt, dot, kt, total;
 };
 // Per-row terms and the transposed fp32 operands are padded to whole 128-row
 // tiles per head (npad rows); the dQ accumulator is not.
@@ -146,11 +147,13 @@ WsLayout ws_layout(int B, int H, int Hkv, int N, int d, int dtype) {
   WsLayout w;
   w.delta = 0;
   w.lse2 = align256(prows * sizeof(float));
-  w.dqacc = w.qt = w.dot = w.kt = 0;
+  w.dqacc = w.fold = w.qt = w.dot = w.kt = 0;
   size_t end = w.lse2 + align256(prows * sizeof(float));
   if (dtype == NEA_BF16) {
     w.dqacc = end;
     end += align256(rows * d * sizeof(float));
+    w.fold = end;  // 2 tiles x 128 rows x 16 bf16 per 128-row query tile
+    end += align256(prows / kTile * 8192);
   } else {
     w.qt = end;
     w.dot = w.qt + align256(prows * d * sizeof(float));
@@ -235,6 +238,7 @@ static int prepare_bwd(BwdArgs* a, const void* Q, const void* K, const void* V, 
   a->delta = reinterpret_cast<float*>(ws + w.delta);
   a->lse2 = reinterpret_cast<float*>(ws + w.lse2);
   a->dq_acc = dtype == NEA_BF16 ? reinterpret_cast<float*>(ws + w.dqacc) : nullptr;
+  a->fold = dtype == NEA_BF16 ? reinterpret_cast<uint16_t*>(ws + w.fold) : nullptr;
   if (dtype == NEA_F32) {
     a->qt = reinterpret_cast<float*>(ws + w.qt);
     a->dot = reinterpret_cast<float*>(ws + w.dot);

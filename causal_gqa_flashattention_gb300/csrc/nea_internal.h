@@ -29,8 +29,11 @@ struct BwdArgs {
   const void* dO;
   const float* lse;                 // [B*H*N]
   float* delta;                     // workspace: D [B*H*N]
-  float* lse2;                      // workspace: LSE * log2(e) [B*H*N]
+  float* lse2;                      // workspace: -LSE * log2(e) [B*H*N]
   float* dq_acc;                    // bf16: fp32 dQ accumulator [B,H,N,d]; fp32: null
+  uint16_t* fold;                   // bf16: per (head, 128-row query tile) two 128 x 16
+                                    // bf16 tiles of row terms for the main kernel's MMAs
+                                    // (-LSE/scale, -D as hi/mid/lo parts); fp32: null
   float* qt;                        // fp32 only: tf32-rounded Q^T  [B*H][d][N]
   float* dot;                       // fp32 only: tf32-rounded dO^T [B*H][d][N]
   float* kt;                        // fp32 only: tf32-rounded K^T  [B*Hkv][d][N]

@@ -16,10 +16,9 @@
 namespace nea {
 namespace {
 
-// D [padded rows] + LSE*log2(e) [padded rows] + fp32 dQ accumulator
-// [rows * d], each rounded up to 256 bytes (padded rows: N rounded up to a
-// multiple of 128 per head).  32 MiB covers, e.g., B*H*N = 98304 rows at
-// d = 64 bf16 (25.9 MB).
+// The layout nea_attn_bwd_workspace_bytes() describes, each part rounded up
+// to 256 bytes (padded rows: N rounded up to a multiple of 128 per head).
+// 32 MiB covers, e.g., B*H*N = 98304 rows at d = 64 bf16 (30.8 MB).
 constexpr size_t kScratchBytes = size_t(32) << 20;
 constexpr int kMaxDevices = 64;
 

@@ -19,6 +19,12 @@ constexpr unsigned int kStatusTimeout = 1u;
 
 // A wait gives up after this many SM clock cycles (about 2 s at 2 GHz).
 constexpr long long kWaitCycles = 4000000000LL;
+// Between checks of the abort flag and the clock, a waiting thread sleeps in
+// mbarrier.try_wait for at most this long; the hardware wakes it as soon as
+// the phase completes.  Spinning instead (try_wait without a hint, a
+// shared-memory read of the abort flag per round) costs shared-memory
+// bandwidth that the tensor core's operand reads need.
+constexpr uint32_t kSuspendNs = 20000;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -47,6 +53,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep up to `ns` nanoseconds first.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Non-blocking: has the phase with the given parity completed?
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -68,7 +87,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kSuspendNs)) return true;
     if (*abort) return false;
     if (clock64() - t0 > kWaitCycles) {
       *abort = 1;
@@ -91,7 +110,7 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, vo
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint32_t id,
                                                 unsigned int* status) {
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, kSuspendNs)) {
     if (clock64() - t0 > kWaitCycles) {
       atomicOr(status, kStatusTimeout | ((id & 0xffu) << 8));
       return false;
@@ -171,6 +190,11 @@ __device__ __forceinline__ void bulk_commit() {
 // Wait until the source smem of all committed bulk groups may be reused.
 __device__ __forceinline__ void bulk_wait_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until the source smem of all but the most recent committed bulk group
+// may be reused.
+__device__ __forceinline__ void bulk_wait_read1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 // Wait until all committed bulk groups have completed (writes visible).
 __device__ __forceinline__ void bulk_wait0() {
@@ -261,6 +285,19 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
   d |= 1ull << 46;
   d |= 2ull << 61;
+  return d;
+}
+
+// Shared-memory matrix descriptor without swizzle, K-major, for a K = 16
+// bf16 operand: 8-row x 16-B core matrices, each 128 contiguous bytes; the
+// two core matrices of a row group (K elements 0-7, 8-15) lie LBO = 128 B
+// apart and row groups SBO = 256 B apart (a 128-row operand is 4 KB).
+__device__ __forceinline__ uint64_t sdesc_k16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(128u >> 4) << 16;
+  d |= static_cast<uint64_t>(256u >> 4) << 32;
+  d |= 1ull << 46;
   return d;
 }
 
@@ -378,6 +415,12 @@ __device__ __forceinline__ uint32_t tf32_rna(float x) {
   uint32_t y;
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
   return y;
+}
+// Element-wise product of two bf16 pairs, rounded to nearest.
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);

@@ -75,9 +75,10 @@ int nea_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LS
 /*
  * Bytes of device workspace nea_attn_bwd() needs for these sizes (256-byte
  * aligned sub-buffers, with Npad = N rounded up to a multiple of 128:
- * D [B*H][Npad] fp32, LSE*log2(e) [B*H][Npad] fp32, then for bf16 the fp32
- * dQ accumulator [B,H,N,d], for fp32 the transposed operands Q^T, dO^T
- * [B*H][d][Npad] and K^T [B*Hkv][d][Npad]).  Returns 0 for invalid or
+ * D [B*H][Npad] fp32, -LSE*log2(e) [B*H][Npad] fp32, then for bf16 the fp32
+ * dQ accumulator [B,H,N,d] and two 4 KB row-term tiles per 128-row query
+ * tile [B*H][Npad/128][2][4096 B], for fp32 the transposed operands Q^T,
+ * dO^T [B*H][d][Npad] and K^T [B*Hkv][d][Npad]).  Returns 0 for invalid or
  * unsupported sizes.
  */
 size_t nea_attn_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d, int dtype);
@@ -114,7 +115,7 @@ int nea_attn_bwd(const void* Q, const void* K, const void* V, const void* O, con
  * nea_attn_bwd().  Arguments mean the same as there.
  *
  * Stage 1, preprocess (HBM-bound): writes scale * rowsum(dO * O) and
- * LSE * log2(e) per row into the workspace and clears the fp32 dQ
+ * -LSE * log2(e) per row into the workspace and clears the fp32 dQ
  * accumulator (for fp32 dtype the accumulator is dQ itself).
  */
 int nea_attn_bwd_preprocess(const void* O, const void* dO, const float* LSE, void* dQ,
@@ -143,15 +144,25 @@ int nea_attn_bwd_finalize(void* dQ, void* workspace, size_t workspace_bytes, int
  * host framework that hands a plugin only its input and output pointers, or
  * a path on which cudaMalloc (which can synchronise the whole device) is not
  * allowed.  Same arguments and results as nea_attn_bwd() minus the
- * workspace; the scratch (D, LSE*log2(e) and the fp32 dQ accumulator) lives
- * in a fixed array of nea_attn_bwd_noalloc_max_bytes() bytes (32 MiB) inside
- * the library, reserved on every GPU that loads it until the process exits.
+ * workspace; the scratch it needs (the layout nea_attn_bwd_workspace_bytes()
+ * describes: for bf16 D, -LSE*log2(e), the fp32 dQ accumulator and the
+ * row-term tiles of the main kernel, about 4*d + 72 bytes per query row;
+ * for fp32 D, -LSE*log2(e) and the transposed Q, dO and K, about
+ * 4*(2d+2) bytes per query row plus 4*d per key row) lives in a fixed
+ * array of nea_attn_bwd_noalloc_max_bytes() bytes (32 MiB) inside the
+ * library.  So bf16 takes up to about 102,000 query rows (B*H*N) at
+ * d = 64 (the GPT-2-small shape, 98,304 rows, fits) and 57,000 at d = 128;
+ * fp32 at d = 64 about 43,000 (H = Hkv) to 55,000 (H = 3 Hkv).
  *   - Sizes whose nea_attn_bwd_workspace_bytes() exceeds that maximum return
  *     NEA_ERR_WORKSPACE and launch nothing.
  *   - No cudaMalloc, cudaFree or other allocating call is made.  The first
  *     call on a device looks up the array's device address there
- *     (cudaGetSymbolAddress) and caches it; make that first call before any
- *     stream capture.
+ *     (cudaGetSymbolAddress) and caches it.  With CUDA's lazy module loading
+ *     (the default) that lookup is also when the runtime loads the part of
+ *     the library that holds the array and reserves its 32 MiB on that
+ *     device, which then stays reserved until the process exits.  Make the
+ *     first call outside any latency-critical path and before any stream
+ *     capture.
  *   - Every call uses the same array, and each call rewrites all of it that
  *     it reads (the dQ accumulator is cleared by the preprocess kernel), so
  *     sequential calls are independent.  Calls that overlap on the GPU (other

@@ -29,6 +29,8 @@
 //            dK and dV stay in TMEM for the whole CTA: the sum over the
 //            group's query heads needs no atomics.
 //  bwd_post  dQ = bf16(-accumulator).
+#include <algorithm>
+
 #include "nea_internal.h"
 #include "ptx.cuh"
 #include "rope.cuh"
@@ -53,19 +55,19 @@ __device__ long long g_trace_bwd[kTraceRoles * kTraceEvents];
 // Walks the per-head rows padded to whole 128-row tiles (npad = T * 128):
 // padded row p = bh * npad + n.  Real rows (n < N) get Ds = scale * dO.O and
 // NL2 = -LSE * log2(e); padding rows get Ds = 0 and NL2 = -inf, so that the
-// backward kernels' exp2(S c + NL2) is exactly 0 for them.  TPR threads per row, each
-// owning 16 bytes of O and dO; every thread handles kPreRows rows with all
-// loads (the row's LSE included) issued before any use, so that a wave of
-// blocks waits for memory once.
+// backward kernels' exp2(S c + NL2) is exactly 0 for them.  TPR threads per
+// row, each owning 16 bytes of O and dO.  A unit of work is kPreRows passes
+// of a block's rows (a divisor of a 128-row tile); every thread issues all
+// loads of its unit (the rows' LSE included) before any use.
 constexpr int kPreRows = 4;
 constexpr int kPreThreads = 256;
 
-// Row terms of the main kernel's S and dP accumulators, as one 16-element
-// K row of a K = 16 MMA operand: x = hi + mid + lo in bf16 (each part the
-// rounded remainder of the previous ones), then zeros.  A tile holds 128
-// query rows in the no-swizzle K-major layout (8-row x 16-B core matrices:
-// row q's first 16 bytes at (q / 8) * 256 + (q % 8) * 16, its second 16 bytes
-// 128 bytes further on).
+// Row terms of the main kernel's S and dP accumulators, as one K row of a
+// K = 16 MMA operand: x = hi + mid + lo in bf16 (each part the rounded
+// remainder of the previous ones), then zeros.  Only the first 16 bytes of
+// each row (K elements 0..7) are stored, row-major: 16 bytes per query row,
+// 2 KB per 128-row tile; the main kernel keeps the zero half in shared
+// memory.
 __device__ __forceinline__ void write_fold_row(uint16_t* tile, int q, float x) {
   const __nv_bfloat16 hi = __float2bfloat16_rn(x);
   const float r1 = x - __bfloat162float(hi);
@@ -76,9 +78,7 @@ __device__ __forceinline__ void write_fold_row(uint16_t* tile, int q, float x) {
          (static_cast<uint32_t>(__bfloat16_as_ushort(mid)) << 16);
   v0.y = static_cast<uint32_t>(__bfloat16_as_ushort(lo));
   v0.z = v0.w = 0u;
-  uint8_t* row = reinterpret_cast<uint8_t*>(tile) + (q / 8) * 256 + (q % 8) * 16;
-  *reinterpret_cast<uint4*>(row) = v0;
-  *reinterpret_cast<uint4*>(row + 128) = make_uint4(0u, 0u, 0u, 0u);
+  *reinterpret_cast<uint4*>(tile + q * 8) = v0;
 }
 
 template <typename T, int D>
@@ -93,80 +93,82 @@ __global__ void __launch_bounds__(kPreThreads) bwd_pre_kernel(const T* __restric
   constexpr int EPV = 16 / sizeof(T);  // elements per 16-B vector
   constexpr int TPR = D / EPV;         // threads per row
   constexpr int RPB = kPreThreads / TPR;  // rows per block per pass
-  static_assert(kTile % (RPB * kPreRows) == 0, "a block's rows must divide a tile");
+  constexpr int UNIT = RPB * kPreRows;    // rows per unit
+  static_assert(kTile % UNIT == 0, "a unit's rows must divide a tile");
   const int sub = threadIdx.x % TPR;
-  // A block's RPB * kPreRows rows divide npad (a multiple of 128), so the
-  // block lies inside one head: bh and the row offset are block-uniform.
-  const long long pb = static_cast<long long>(blockIdx.x) * RPB * kPreRows;
-  const long long bh = pb / npad;
-  const int nb = static_cast<int>(pb - bh * npad) + threadIdx.x / TPR;
-  const long long p0 = pb + threadIdx.x / TPR;
-  uint4 ov[kPreRows], gv[kPreRows];
-  float lv[kPreRows];
-  long long rrow[kPreRows];  // unpadded row index, or -1 for padding / past the end
+  const long long units = prows / UNIT;
+  for (long long unit = blockIdx.x; unit < units; unit += gridDim.x) {
+    // A unit lies inside one head: bh and the row offset are unit-uniform.
+    const long long pb = unit * UNIT;
+    const long long bh = pb / npad;
+    const int nb = static_cast<int>(pb - bh * npad) + threadIdx.x / TPR;
+    const long long p0 = pb + threadIdx.x / TPR;
+    uint4 ov[kPreRows], gv[kPreRows];
+    float lv[kPreRows];
+    long long rrow[kPreRows];  // unpadded row index, or -1 for padding
 #pragma unroll
-  for (int u = 0; u < kPreRows; ++u) {
-    const long long p = p0 + static_cast<long long>(u) * RPB;
-    const int n = nb + u * RPB;
-    rrow[u] = (p < prows && n < N) ? bh * N + n : -1;
-    lv[u] = 0.f;
-    if (rrow[u] >= 0) {
-      const size_t base = static_cast<size_t>(rrow[u]) * D + sub * EPV;
-      ov[u] = __ldg(reinterpret_cast<const uint4*>(O + base));
-      gv[u] = __ldg(reinterpret_cast<const uint4*>(dO + base));
-      if (sub == 0) lv[u] = __ldg(lse + rrow[u]);
-    } else {
-      ov[u] = gv[u] = make_uint4(0, 0, 0, 0);
-    }
-  }
-#pragma unroll
-  for (int u = 0; u < kPreRows; ++u) {
-    const long long p = p0 + static_cast<long long>(u) * RPB;
-    float acc = 0.f;
-    if constexpr (sizeof(T) == 2) {
-      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov[u]);
-      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv[u]);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 x = __bfloat1622float2(o2[k]), y = __bfloat1622float2(g2[k]);
-        acc = fmaf(x.x, y.x, acc);
-        acc = fmaf(x.y, y.y, acc);
-      }
-    } else {
-      const float* o4 = reinterpret_cast<const float*>(&ov[u]);
-      const float* g4 = reinterpret_cast<const float*>(&gv[u]);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) acc = fmaf(o4[k], g4[k], acc);
-    }
-    // every lane of the warp runs the shuffle (padding rows add zeros)
-#pragma unroll
-    for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (p < prows && sub == 0) {
-      ds_row[p] = rrow[u] >= 0 ? acc * scale : 0.f;
-      l2_row[p] = rrow[u] >= 0 ? -lv[u] * kLog2e : -INFINITY;
-      if (fold != nullptr) {
-        // tile p / 128 = (head, query tile): S' = S - LSE / scale (padding:
-        // -1e30, so that P = 0 there), then dP' = dP - D
-        uint16_t* tile = fold + (p / kTile) * 4096;
-        const int q = static_cast<int>(p % kTile);
-        write_fold_row(tile, q, rrow[u] >= 0 ? -lv[u] / scale : -1e30f);
-        write_fold_row(tile + 2048, q, rrow[u] >= 0 ? -acc : 0.f);
+    for (int u = 0; u < kPreRows; ++u) {
+      const int n = nb + u * RPB;
+      rrow[u] = n < N ? bh * N + n : -1;
+      lv[u] = 0.f;
+      if (rrow[u] >= 0) {
+        const size_t base = static_cast<size_t>(rrow[u]) * D + sub * EPV;
+        ov[u] = __ldg(reinterpret_cast<const uint4*>(O + base));
+        gv[u] = __ldg(reinterpret_cast<const uint4*>(dO + base));
+        if (sub == 0) lv[u] = __ldg(lse + rrow[u]);
+      } else {
+        ov[u] = gv[u] = make_uint4(0, 0, 0, 0);
       }
     }
-    // zero this thread's share of the fp32 accumulator row (D floats)
-    if (dq_acc != nullptr && rrow[u] >= 0) {
-      float4* z = reinterpret_cast<float4*>(dq_acc + static_cast<size_t>(rrow[u]) * D);
 #pragma unroll
-      for (int k = sub; k < D / 4; k += TPR) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int u = 0; u < kPreRows; ++u) {
+      const long long p = p0 + static_cast<long long>(u) * RPB;
+      float acc = 0.f;
+      if constexpr (sizeof(T) == 2) {
+        const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov[u]);
+        const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv[u]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 x = __bfloat1622float2(o2[k]), y = __bfloat1622float2(g2[k]);
+          acc = fmaf(x.x, y.x, acc);
+          acc = fmaf(x.y, y.y, acc);
+        }
+      } else {
+        const float* o4 = reinterpret_cast<const float*>(&ov[u]);
+        const float* g4 = reinterpret_cast<const float*>(&gv[u]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc = fmaf(o4[k], g4[k], acc);
+      }
+      // every lane of the warp runs the shuffle (padding rows add zeros)
+#pragma unroll
+      for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (sub == 0) {
+        ds_row[p] = rrow[u] >= 0 ? acc * scale : 0.f;
+        l2_row[p] = rrow[u] >= 0 ? -lv[u] * kLog2e : -INFINITY;
+        if (fold != nullptr) {
+          // tile pair p / 128 = (head, query tile): S' = S - LSE / scale
+          // (padding: -1e30, so that P = 0 there), then dP' = dP - D
+          uint16_t* tile = fold + (p / kTile) * 2048;
+          const int q = static_cast<int>(p % kTile);
+          write_fold_row(tile, q, rrow[u] >= 0 ? -lv[u] / scale : -1e30f);
+          write_fold_row(tile + 1024, q, rrow[u] >= 0 ? -acc : 0.f);
+        }
+      }
+      // zero this thread's share of the fp32 accumulator row (D floats)
+      if (dq_acc != nullptr && rrow[u] >= 0) {
+        float4* z = reinterpret_cast<float4*>(dq_acc + static_cast<size_t>(rrow[u]) * D);
+#pragma unroll
+        for (int k = sub; k < D / 4; k += TPR) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
   }
 }
 
 // ---------------------------------------------------------------- dQ cast
-// Each thread converts kPostVecs groups of 8 fp32 -> 8 bf16.  The main
-// kernel accumulates -dQ (see its sign convention), so the cast negates.
-// With a RoPE table, the 4 pairs of a group are first turned back by their
-// row's angles.
+// Each thread converts kPostVecs groups of 8 fp32 -> 8 bf16 per round.  The
+// main kernel accumulates -dQ (see
+// its sign convention), so the cast negates.  With a RoPE table, the 4 pairs
+// of a group are first turned back by their row's angles.
 constexpr int kPostVecs = 4;
 constexpr int kPostThreads = 256;
 
@@ -175,42 +177,45 @@ __global__ void __launch_bounds__(kPostThreads) bwd_post_kernel(const float* __r
                                                        long long n8,
                                                        const float2* __restrict__ cs, int N,
                                                        int d) {
-  const long long i0 = static_cast<long long>(blockIdx.x) * kPostThreads * kPostVecs + threadIdx.x;
-  float4 a[kPostVecs], b[kPostVecs];
-#pragma unroll
-  for (int u = 0; u < kPostVecs; ++u) {
-    const long long i = i0 + static_cast<long long>(u) * kPostThreads;
-    if (i < n8) {
-      a[u] = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i);
-      b[u] = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i + 1);
-    }
-  }
-  if (cs != nullptr) {
+  const long long per_round = static_cast<long long>(gridDim.x) * kPostThreads * kPostVecs;
+  for (long long i0 = static_cast<long long>(blockIdx.x) * kPostThreads * kPostVecs + threadIdx.x;
+       i0 < n8; i0 += per_round) {
+    float4 a[kPostVecs], b[kPostVecs];
 #pragma unroll
     for (int u = 0; u < kPostVecs; ++u) {
       const long long i = i0 + static_cast<long long>(u) * kPostThreads;
       if (i < n8) {
-        const long long e = 8 * i;  // first element of the group; d % 8 == 0
-        const long long row = e / d;
-        const int col = static_cast<int>(e - row * d);
-        const float2* t = cs + static_cast<size_t>(row % N) * (d / 2) + col / 2;
-        rope_inv(a[u].x, a[u].y, __ldg(t));
-        rope_inv(a[u].z, a[u].w, __ldg(t + 1));
-        rope_inv(b[u].x, b[u].y, __ldg(t + 2));
-        rope_inv(b[u].z, b[u].w, __ldg(t + 3));
+        a[u] = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i);
+        b[u] = __ldg(reinterpret_cast<const float4*>(acc) + 2 * i + 1);
       }
     }
-  }
+    if (cs != nullptr) {
 #pragma unroll
-  for (int u = 0; u < kPostVecs; ++u) {
-    const long long i = i0 + static_cast<long long>(u) * kPostThreads;
-    if (i < n8) {
-      uint4 v;
-      v.x = pack_bf16(-a[u].x, -a[u].y);
-      v.y = pack_bf16(-a[u].z, -a[u].w);
-      v.z = pack_bf16(-b[u].x, -b[u].y);
-      v.w = pack_bf16(-b[u].z, -b[u].w);
-      reinterpret_cast<uint4*>(dq)[i] = v;
+      for (int u = 0; u < kPostVecs; ++u) {
+        const long long i = i0 + static_cast<long long>(u) * kPostThreads;
+        if (i < n8) {
+          const long long e = 8 * i;  // first element of the group; d % 8 == 0
+          const long long row = e / d;
+          const int col = static_cast<int>(e - row * d);
+          const float2* t = cs + static_cast<size_t>(row % N) * (d / 2) + col / 2;
+          rope_inv(a[u].x, a[u].y, __ldg(t));
+          rope_inv(a[u].z, a[u].w, __ldg(t + 1));
+          rope_inv(b[u].x, b[u].y, __ldg(t + 2));
+          rope_inv(b[u].z, b[u].w, __ldg(t + 3));
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kPostVecs; ++u) {
+      const long long i = i0 + static_cast<long long>(u) * kPostThreads;
+      if (i < n8) {
+        uint4 v;
+        v.x = pack_bf16(-a[u].x, -a[u].y);
+        v.y = pack_bf16(-a[u].z, -a[u].w);
+        v.z = pack_bf16(-b[u].x, -b[u].y);
+        v.w = pack_bf16(-b[u].z, -b[u].w);
+        reinterpret_cast<uint4*>(dq)[i] = v;
+      }
     }
   }
 }
@@ -250,7 +255,10 @@ struct BwdCfg {
   static constexpr int OFF_DS = OFF_DO + DOST * TILE_BYTES;  // DSST x (128x128 bf16, 2 blocks)
   static constexpr int OFF_DQ = OFF_DS + DSST * 2 * BLK_BYTES;  // one fp32 box of 128x32
   // K = 16 operands of the row-term MMAs (4 KB each): the ones tile, and per
-  // ring stage the query tile's -LSE/scale (with Q) and -D (with dO) tiles
+  // ring stage the query tile's -LSE/scale (with Q) and -D (with dO) tiles.
+  // Each holds K elements 0..7 of its 128 rows in its first 2 KB (row r at
+  // r * 16) and zeros (K elements 8..15) in the second: the no-swizzle
+  // K-major layout with core matrices 128 B apart along M/N, 2 KB along K.
   static constexpr int FOLD_BYTES = 4096;
   static constexpr int OFF_ONES = OFF_DQ + BLK_BYTES;
   static constexpr int OFF_FU = OFF_ONES + FOLD_BYTES;
@@ -369,13 +377,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
     tmem_alloc(smem_u32(&tmem_base_sh), 512);
     tmem_relinquish();
   }
-  // the ones operand of the row-term MMAs: every key row = (1, 1, 1, 0, ..., 0)
-  if (threadIdx.x < 256) {
-    const int r = threadIdx.x >> 1, half16 = threadIdx.x & 1;
-    *reinterpret_cast<uint4*>(smem + C::OFF_ONES + (r / 8) * 256 + half16 * 128 + (r % 8) * 16) =
-        half16 == 0 ? make_uint4(0x3F803F80u, 0x00003F80u, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
-    fence_proxy_async();
+  // the ones operand of the row-term MMAs (every key row = (1, 1, 1, 0, ...,
+  // 0)) and the zero halves of the ring's row-term tiles
+  for (int c = threadIdx.x; c < (1 + QST + DOST) * 128; c += blockDim.x) {
+    const int t = c / 128, r = c % 128;
+    uint8_t* tile = smem + (t == 0 ? C::OFF_ONES : t <= QST ? C::OFF_FU + (t - 1) * C::FOLD_BYTES
+                                                            : C::OFF_FW + (t - 1 - QST) * C::FOLD_BYTES);
+    if (t == 0)
+      *reinterpret_cast<uint4*>(tile + r * 16) = make_uint4(0x3F803F80u, 0x00003F80u, 0u, 0u);
+    *reinterpret_cast<uint4*>(tile + 2048 + r * 16) = make_uint4(0u, 0u, 0u, 0u);
   }
+  fence_proxy_async();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -390,22 +402,26 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
   const bool traced = blockIdx.x == 0 && lane == 0;
   if (warp == 0) {
     // ------------------------------------------------------------ producer + dQ issuer
-    // One thread runs two roles without blocking on either: it issues
+    // One warp runs two roles without blocking on either: it issues
     // dQ'_n = dS'_n K_j (A = the same shared-memory bytes as dS'^T, read
     // MN-major) as soon as dS'^T_n is in shared memory and the drain warps
     // have read dQ'_{n-1} out of TMEM, and it keeps the Q and dO rings
-    // full.  The dQ MMAs go first: they are on the critical path,
-    // the loads run ahead of their use.
-    if (lane == 0) {
+    // full.  The dQ MMAs go first: they are on the critical path, the loads
+    // run ahead of their use.  The whole warp runs the loop (its tests are
+    // warp-uniform); one elected lane issues the copies, MMAs and commits.
+    {
       Tracer tr(NEA_TRACE_BASE, traced, 0);
       Tracer trq(NEA_TRACE_BASE, traced, 7);
       tr.ev(0);
       const int kvh = b * a.Hkv + g;
-      mbar_expect_tx(bar(C_KVFULL), 2 * C::TILE_BYTES);
-      for (int k = 0; k < C::NBLK; ++k) {
-        tma_load_3d(sK + k * C::BLK_BYTES, &a.tmK, bar(C_KVFULL), k * 64, j * kTile, kvh);
-        tma_load_3d(sV + k * C::BLK_BYTES, &a.tmV, bar(C_KVFULL), k * 64, j * kTile, kvh);
+      if (elect_one()) {
+        mbar_expect_tx(bar(C_KVFULL), 2 * C::TILE_BYTES);
+        for (int k = 0; k < C::NBLK; ++k) {
+          tma_load_3d(sK + k * C::BLK_BYTES, &a.tmK, bar(C_KVFULL), k * 64, j * kTile, kvh);
+          tma_load_3d(sV + k * C::BLK_BYTES, &a.tmV, bar(C_KVFULL), k * 64, j * kTile, kvh);
+        }
       }
+      __syncwarp();
       constexpr uint32_t idDQ = make_idesc<MmaKind::kBF16>(128, D, true, true);
       int nl = 0, nd = 0, nq = DQ ? 0 : nsteps;  // next step to load Q / dO / issue dQ for
       bool ok = true;
@@ -414,35 +430,41 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
         bool progress = false;
         if (nq < nsteps) {
           const int bb = nq % DSST;
-          if (mbar_test(dsfull(bb), (nq / DSST) & 1) &&
-              (nq == 0 || mbar_test(bar(C_DQFREE), (nq - 1) & 1))) {
+          if (mbar_test_warp(dsfull(bb), (nq / DSST) & 1) &&
+              (nq == 0 || mbar_test_warp(bar(C_DQFREE), (nq - 1) & 1))) {
             trq.ev(22);
             tc_fence_after();
+            if (elect_one()) {
 #pragma unroll
-            for (int k = 0; k < C::NK_T; ++k)
-              mma_ss<MmaKind::kBF16>(tmem + C::DQ_COL,
-                                     sdesc_sw128(sDS(bb) + k * 16 * 128, C::BLK_BYTES, 1024),
-                                     sdesc_sw128(sK + k * 16 * 128, C::BLK_BYTES, 1024), idDQ,
-                                     k > 0 ? 1u : 0u);
-            mma_commit(dsempty(bb));
-            mma_commit(bar(C_DQFULL));
+              for (int k = 0; k < C::NK_T; ++k)
+                mma_ss<MmaKind::kBF16>(tmem + C::DQ_COL,
+                                       sdesc_sw128(sDS(bb) + k * 16 * 128, C::BLK_BYTES, 1024),
+                                       sdesc_sw128(sK + k * 16 * 128, C::BLK_BYTES, 1024), idDQ,
+                                       k > 0 ? 1u : 0u);
+              mma_commit(dsempty(bb));
+              mma_commit(bar(C_DQFULL));
+            }
+            __syncwarp();
             trq.ev(23);
             ++nq;
             progress = true;
           }
         }
-        // the two row-term tiles of (head, query tile): 8 KB per tile in the workspace
+        // the two row-term tiles of (head, query tile): 2 KB each in the workspace
         if (nl < nsteps) {
           const int s = nl % QST;
-          if (nl < QST || mbar_test(qempty(s), ((nl / QST) - 1) & 1)) {
+          if (nl < QST || mbar_test_warp(qempty(s), ((nl / QST) - 1) & 1)) {
             int h, i;
             step_hi(nl, h, i);
             const int bh = b * a.H + h;
-            const uint16_t* fold = a.fold + (static_cast<size_t>(bh) * T + i) * 4096;
-            mbar_expect_tx(qfull(s), C::TILE_BYTES + C::FOLD_BYTES);
-            for (int k = 0; k < C::NBLK; ++k)
-              tma_load_3d(sQ(s) + k * C::BLK_BYTES, &a.tmQ, qfull(s), k * 64, i * kTile, bh);
-            bulk_load(sFU(s), fold, C::FOLD_BYTES, qfull(s));
+            const uint16_t* fold = a.fold + (static_cast<size_t>(bh) * T + i) * 2048;
+            if (elect_one()) {
+              mbar_expect_tx(qfull(s), C::TILE_BYTES + 2048);
+              for (int k = 0; k < C::NBLK; ++k)
+                tma_load_3d(sQ(s) + k * C::BLK_BYTES, &a.tmQ, qfull(s), k * 64, i * kTile, bh);
+              bulk_load(sFU(s), fold, 2048, qfull(s));
+            }
+            __syncwarp();
             tr.ev(1);
             ++nl;
             progress = true;
@@ -450,15 +472,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
         }
         if (nd < nsteps) {
           const int s = nd % DOST;
-          if (nd < DOST || mbar_test(doempty(s), ((nd / DOST) - 1) & 1)) {
+          if (nd < DOST || mbar_test_warp(doempty(s), ((nd / DOST) - 1) & 1)) {
             int h, i;
             step_hi(nd, h, i);
             const int bh = b * a.H + h;
-            const uint16_t* fold = a.fold + (static_cast<size_t>(bh) * T + i) * 4096;
-            mbar_expect_tx(dofull(s), C::TILE_BYTES + C::FOLD_BYTES);
-            for (int k = 0; k < C::NBLK; ++k)
-              tma_load_3d(sDO(s) + k * C::BLK_BYTES, &a.tmdO, dofull(s), k * 64, i * kTile, bh);
-            bulk_load(sFW(s), fold + 2048, C::FOLD_BYTES, dofull(s));
+            const uint16_t* fold = a.fold + (static_cast<size_t>(bh) * T + i) * 2048;
+            if (elect_one()) {
+              mbar_expect_tx(dofull(s), C::TILE_BYTES + 2048);
+              for (int k = 0; k < C::NBLK; ++k)
+                tma_load_3d(sDO(s) + k * C::BLK_BYTES, &a.tmdO, dofull(s), k * 64, i * kTile, bh);
+              bulk_load(sFW(s), fold + 1024, 2048, dofull(s));
+            }
+            __syncwarp();
             ++nd;
             progress = true;
           }
@@ -468,21 +493,27 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
           continue;
         }
         // nothing ready: back off briefly; give up with the other roles
-        if (*abort) {
-          ok = false;
-          break;
+        // (lane 0 decides for the warp)
+        int give_up = 0;
+        if (lane == 0) {
+          if (*abort) {
+            give_up = 1;
+          } else if (clock64() - idle0 > kWaitCycles) {
+            *abort = 1;
+            atomicOr(status, kStatusTimeout | (20u << 8));
+            give_up = 1;
+          }
         }
-        if (clock64() - idle0 > kWaitCycles) {
-          *abort = 1;
-          atomicOr(status, kStatusTimeout | (20u << 8));
+        if (__shfl_sync(0xffffffffu, give_up, 0)) {
           ok = false;
           break;
         }
         __nanosleep(32);
       }
-      // everything this thread started must finish before the CTA exits:
-      // its MMAs, and (when unwinding) the loads it issued
-      mma_commit(bar(C_DRAIN4));
+      // everything this warp started must finish before the CTA exits: its
+      // MMAs, and (when unwinding) the loads it issued
+      if (elect_one()) mma_commit(bar(C_DRAIN4));
+      __syncwarp();
       mbar_wait_drain(bar(C_DRAIN4), 0, 41, status);
       mbar_wait_drain(bar(C_KVFULL), 0, 21, status);
       if (!ok) {
@@ -494,114 +525,135 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ issuer 1: S^T, dP^T
-    // One thread issues a tcgen05.mma about every ~120 cycles whatever its
-    // size, so the five GEMMs of a step are spread over four issuing warps
-    // (S^T and dP^T here; dV, dK and dQ each on a warp of its own).  Every
-    // hazard between issuers goes through an mbarrier.
-    if (lane == 0) {
+    // The five GEMMs of a step are spread over four issuing warps (S^T and
+    // dP^T here; dV, dK and dQ each on a warp of its own), so that the
+    // tensor core always has work queued.  Every hazard between issuers
+    // goes through an mbarrier.  Each issuing warp runs its loop converged
+    // (warp-uniform waits) and issues from one elected lane.
+    {
       Tracer tr(NEA_TRACE_BASE, traced, 1);
       constexpr uint32_t idS = make_idesc<MmaKind::kBF16>(128, 128, false, false);
-      bool ok = mbar_wait(bar(C_KVFULL), 0, abort, 22, status);
+      bool ok = mbar_wait_warp(bar(C_KVFULL), 0, abort, 22, status);
       for (int n = 0; ok && n < nsteps; ++n) {
         const int s = n % QST, sd = n % DOST;
         const uint32_t ph = (n / QST) & 1, phd = (n / DOST) & 1;
         // S^T_n = K_j Q_i^T: Q_n has landed; the compute warps have read S^T_{n-1}
         // (and, with P in S's columns, dV_{n-1} has read P^T_{n-1})
-        ok = mbar_wait(qfull(s), ph, abort, 23, status) &&
-             (n == 0 || mbar_wait(bar(C_SFREE), (n - 1) & 1, abort, 24, status)) &&
-             (!C::P_ALIAS_S || n == 0 || mbar_wait(bar(C_PFREE), (n - 1) & 1, abort, 24, status));
+        ok = mbar_wait_warp(qfull(s), ph, abort, 23, status) &&
+             (n == 0 || mbar_wait_warp(bar(C_SFREE), (n - 1) & 1, abort, 24, status)) &&
+             (!C::P_ALIAS_S || n == 0 ||
+              mbar_wait_warp(bar(C_PFREE), (n - 1) & 1, abort, 24, status));
         if (!ok) break;
         tr.ev(12);
         tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < C::NK_QK; ++k) {
-          const uint32_t off = (k / 4) * C::BLK_BYTES + (k % 4) * 32;
-          mma_ss<MmaKind::kBF16>(tmem + C::S_COL, sdesc_sw128(sK + off, 16, 1024),
-                                 sdesc_sw128(sQ(s) + off, 16, 1024), idS, k > 0 ? 1u : 0u);
+          for (int k = 0; k < C::NK_QK; ++k) {
+            const uint32_t off = (k / 4) * C::BLK_BYTES + (k % 4) * 32;
+            mma_ss<MmaKind::kBF16>(tmem + C::S_COL, sdesc_sw128(sK + off, 16, 1024),
+                                   sdesc_sw128(sQ(s) + off, 16, 1024), idS, k > 0 ? 1u : 0u);
+          }
+          // S'^T = S^T + 1 u^T, u = -LSE / scale of each query (one K = 16 step)
+          mma_ss<MmaKind::kBF16>(tmem + C::S_COL, sdesc_k16(sONES), sdesc_k16(sFU(s)), idS, 1u);
+          mma_commit(bar(C_SFULL));
+          mma_commit(qempty(s));  // Q_n no longer read by this issuer
         }
-        // S'^T = S^T + 1 u^T, u = -LSE / scale of each query (one K = 16 step)
-        mma_ss<MmaKind::kBF16>(tmem + C::S_COL, sdesc_k16(sONES), sdesc_k16(sFU(s)), idS, 1u);
-        mma_commit(bar(C_SFULL));
-        mma_commit(qempty(s));  // Q_n no longer read by this issuer
+        __syncwarp();
         tr.ev(13);
         // dP^T_n = V_j dO_i^T: dO_n has landed; dP^T_{n-1} has been read (and,
         // with dQ in dP's columns, dQ_{n-1} has been drained)
-        ok = mbar_wait(dofull(sd), phd, abort, 25, status) &&
-             (n == 0 || mbar_wait(bar(C_DPFREE), (n - 1) & 1, abort, 25, status)) &&
+        ok = mbar_wait_warp(dofull(sd), phd, abort, 25, status) &&
+             (n == 0 || mbar_wait_warp(bar(C_DPFREE), (n - 1) & 1, abort, 25, status)) &&
              (!(DQ && C::DQ_ALIAS_DP) || n == 0 ||
-              mbar_wait(bar(C_DQFREE), (n - 1) & 1, abort, 25, status));
+              mbar_wait_warp(bar(C_DQFREE), (n - 1) & 1, abort, 25, status));
         if (!ok) break;
         tr.ev(14);
         tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < C::NK_QK; ++k) {
-          const uint32_t off = (k / 4) * C::BLK_BYTES + (k % 4) * 32;
-          mma_ss<MmaKind::kBF16>(tmem + C::DP_COL, sdesc_sw128(sV + off, 16, 1024),
-                                 sdesc_sw128(sDO(sd) + off, 16, 1024), idS, k > 0 ? 1u : 0u);
+          for (int k = 0; k < C::NK_QK; ++k) {
+            const uint32_t off = (k / 4) * C::BLK_BYTES + (k % 4) * 32;
+            mma_ss<MmaKind::kBF16>(tmem + C::DP_COL, sdesc_sw128(sV + off, 16, 1024),
+                                   sdesc_sw128(sDO(sd) + off, 16, 1024), idS, k > 0 ? 1u : 0u);
+          }
+          // dP'^T = dP^T - 1 D^T (one K = 16 step)
+          mma_ss<MmaKind::kBF16>(tmem + C::DP_COL, sdesc_k16(sONES), sdesc_k16(sFW(sd)), idS, 1u);
+          mma_commit(bar(C_DPFULL));
+          mma_commit(doempty(sd));  // dO_n no longer read by this issuer
         }
-        // dP'^T = dP^T - 1 D^T (one K = 16 step)
-        mma_ss<MmaKind::kBF16>(tmem + C::DP_COL, sdesc_k16(sONES), sdesc_k16(sFW(sd)), idS, 1u);
-        mma_commit(bar(C_DPFULL));
-        mma_commit(doempty(sd));  // dO_n no longer read by this issuer
+        __syncwarp();
         tr.ev(15);
       }
-      mma_commit(bar(C_DRAIN1));
+      if (elect_one()) mma_commit(bar(C_DRAIN1));
+      __syncwarp();
       mbar_wait_drain(bar(C_DRAIN1), 0, 29, status);
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ issuer 2: dV
-    if (lane == 0) {
+    {
       Tracer tr(NEA_TRACE_BASE, traced, 2);
       constexpr uint32_t idDV = make_idesc<MmaKind::kBF16>(128, D, false, true);
       bool ok = true;
       for (int n = 0; ok && n < nsteps; ++n) {
         const int s = n % DOST;
         // dV += P^T_n dO_n (P^T from tensor memory)
-        ok = mbar_wait(dofull(s), (n / DOST) & 1, abort, 26, status) &&
-             mbar_wait(bar(C_PFULL), n & 1, abort, 26, status);
+        ok = mbar_wait_warp(dofull(s), (n / DOST) & 1, abort, 26, status) &&
+             mbar_wait_warp(bar(C_PFULL), n & 1, abort, 26, status);
         if (!ok) break;
         tr.ev(10);
         tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < C::NK_T; ++k)
-          mma_ts<MmaKind::kBF16>(tmem + C::DV_COL, tmem + p_col(k),
-                                 sdesc_sw128(sDO(s) + k * 16 * 128, C::BLK_BYTES, 1024), idDV,
-                                 (n > 0 || k > 0) ? 1u : 0u);
-        mma_commit(bar(C_PFREE));
-        mma_commit(doempty(s));
+          for (int k = 0; k < C::NK_T; ++k)
+            mma_ts<MmaKind::kBF16>(tmem + C::DV_COL, tmem + p_col(k),
+                                   sdesc_sw128(sDO(s) + k * 16 * 128, C::BLK_BYTES, 1024), idDV,
+                                   (n > 0 || k > 0) ? 1u : 0u);
+          mma_commit(bar(C_PFREE));
+          mma_commit(doempty(s));
+        }
+        __syncwarp();
         tr.ev(11);
       }
-      mma_commit(bar(C_FINAL));
-      mma_commit(bar(C_DRAIN2));
+      if (elect_one()) {
+        mma_commit(bar(C_FINAL));
+        mma_commit(bar(C_DRAIN2));
+      }
+      __syncwarp();
       mbar_wait_drain(bar(C_DRAIN2), 0, 39, status);
     }
   } else if (warp == 3) {
     // ------------------------------------------------------------ issuer 3: dK
-    if (lane == 0) {
+    {
       Tracer tr(NEA_TRACE_BASE, traced, 3);
       constexpr uint32_t idDK = make_idesc<MmaKind::kBF16>(128, D, false, true);
       bool ok = true;
       for (int n = 0; ok && n < nsteps; ++n) {
         const int s = n % QST, bb = n % DSST;
         // dK' += dS'^T_n Q_n
-        ok = mbar_wait(qfull(s), (n / QST) & 1, abort, 38, status) &&
-             mbar_wait(dsfull(bb), (n / DSST) & 1, abort, 27, status);
+        ok = mbar_wait_warp(qfull(s), (n / QST) & 1, abort, 38, status) &&
+             mbar_wait_warp(dsfull(bb), (n / DSST) & 1, abort, 27, status);
         if (!ok) break;
         tr.ev(20);
         tc_fence_after();
+        if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < C::NK_T; ++k) {
-          const uint32_t off = (k / 4) * C::BLK_BYTES + (k % 4) * 32;
-          mma_ss<MmaKind::kBF16>(tmem + C::DK_COL, sdesc_sw128(sDS(bb) + off, 16, 1024),
-                                 sdesc_sw128(sQ(s) + k * 16 * 128, C::BLK_BYTES, 1024), idDK,
-                                 (n > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < C::NK_T; ++k) {
+            const uint32_t off = (k / 4) * C::BLK_BYTES + (k % 4) * 32;
+            mma_ss<MmaKind::kBF16>(tmem + C::DK_COL, sdesc_sw128(sDS(bb) + off, 16, 1024),
+                                   sdesc_sw128(sQ(s) + k * 16 * 128, C::BLK_BYTES, 1024), idDK,
+                                   (n > 0 || k > 0) ? 1u : 0u);
+          }
+          mma_commit(dsempty(bb));
+          mma_commit(qempty(s));
         }
-        mma_commit(dsempty(bb));
-        mma_commit(qempty(s));
+        __syncwarp();
         tr.ev(21);
       }
-      mma_commit(bar(C_FINAL));
-      mma_commit(bar(C_DRAIN3));
+      if (elect_one()) {
+        mma_commit(bar(C_FINAL));
+        mma_commit(bar(C_DRAIN3));
+      }
+      __syncwarp();
       mbar_wait_drain(bar(C_DRAIN3), 0, 40, status);
     }
   } else if (warp >= 4 && warp < C::DQ_WARP0) {
@@ -868,23 +920,25 @@ cudaError_t launch_main_t(const BwdArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t stream) {
+cudaError_t launch_bwd_pre(const BwdArgs& a, int sms, cudaStream_t stream) {
   const int npad = (a.N + kTile - 1) / kTile * kTile;
   const long long prows = static_cast<long long>(a.B) * a.H * npad;
   const int esize = a.dtype == 0 ? 2 : 4;
   const int tpr = a.d * esize / 16;
-  const long long per_block = static_cast<long long>(kPreThreads / tpr) * kPreRows;  // divides 128
-  const unsigned grid = static_cast<unsigned>((prows + per_block - 1) / per_block);
+  const long long units = prows / (static_cast<long long>(kPreThreads / tpr) * kPreRows);
+  // one block per unit: more blocks than fit at once keep more loads in flight
+  (void)sms;
+  auto grid_for = [&](auto) { return static_cast<unsigned>(units); };
   if (a.dtype == 0 && a.d == 64)
-    bwd_pre_kernel<__nv_bfloat16, 64><<<grid, kPreThreads, 0, stream>>>(
+    bwd_pre_kernel<__nv_bfloat16, 64><<<grid_for(bwd_pre_kernel<__nv_bfloat16, 64>), kPreThreads, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(a.O), static_cast<const __nv_bfloat16*>(a.dO), a.lse,
         a.delta, a.lse2, a.dq_acc, a.fold, prows, a.N, npad, a.scale);
   else if (a.dtype == 0 && a.d == 128)
-    bwd_pre_kernel<__nv_bfloat16, 128><<<grid, kPreThreads, 0, stream>>>(
+    bwd_pre_kernel<__nv_bfloat16, 128><<<grid_for(bwd_pre_kernel<__nv_bfloat16, 128>), kPreThreads, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(a.O), static_cast<const __nv_bfloat16*>(a.dO), a.lse,
         a.delta, a.lse2, a.dq_acc, a.fold, prows, a.N, npad, a.scale);
   else if (a.dtype == 1 && a.d == 64)
-    bwd_pre_kernel<float, 64><<<grid, kPreThreads, 0, stream>>>(
+    bwd_pre_kernel<float, 64><<<grid_for(bwd_pre_kernel<float, 64>), kPreThreads, 0, stream>>>(
         static_cast<const float*>(a.O), static_cast<const float*>(a.dO), a.lse, a.delta, a.lse2,
         a.dq_acc, nullptr, prows, a.N, npad, a.scale);
   else
@@ -901,11 +955,12 @@ cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream) {
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_bwd_post(const BwdArgs& a, cudaStream_t stream) {
+cudaError_t launch_bwd_post(const BwdArgs& a, int sms, cudaStream_t stream) {
   const long long n8 = static_cast<long long>(a.B) * a.H * a.N * a.d / 8;
   const long long per_block = static_cast<long long>(kPostThreads) * kPostVecs;
-  bwd_post_kernel<<<static_cast<unsigned>((n8 + per_block - 1) / per_block), kPostThreads, 0,
-                    stream>>>(
+  (void)sms;
+  const long long blocks = (n8 + per_block - 1) / per_block;
+  bwd_post_kernel<<<static_cast<unsigned>(blocks), kPostThreads, 0, stream>>>(
       a.dq_acc, static_cast<__nv_bfloat16*>(a.dQ), n8, a.rope_cs, a.N, a.d);
   return cudaGetLastError();
 }

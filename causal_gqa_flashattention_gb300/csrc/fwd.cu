@@ -251,7 +251,9 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the issue loop (waits are warp-uniform); one
+    // elected lane issues each burst of MMAs and its commits.
+    {
       constexpr uint32_t idS = make_idesc<KIND>(128, 128, false, false);
       constexpr uint32_t idPV = make_idesc<KIND>(128, D, false, !C::TRANSPOSE_V);
       const int qbar = C::TRANSPOSE_V ? B_QREADY : B_QFULL;
@@ -260,23 +262,26 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
       auto issue_s = [&](int g, const FwdItem& it, int j) -> bool {
         const int s = g % ST;
         const int kbar = C::TRANSPOSE_V ? B_KFULL + 4 * ST + s : B_KFULL + s;
-        if (!mbar_wait(bar(kbar), (g / ST) & 1, abort, 3, status)) return false;
+        if (!mbar_wait_warp(bar(kbar), (g / ST) & 1, abort, 3, status)) return false;
         tc_fence_after();
         const uint32_t sK = sKV + (2 * s) * C::TILE_BYTES;
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < C::NK_QK; ++kk) {
-          const uint32_t off = ((kk * 32) / 128) * C::BLK_BYTES + (kk * 32) % 128;
-          mma_ss<KIND>(tmem + C::S_COL, sdesc_sw128(sQ + off, 16, 1024),
-                       sdesc_sw128(sK + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < C::NK_QK; ++kk) {
+            const uint32_t off = ((kk * 32) / 128) * C::BLK_BYTES + (kk * 32) % 128;
+            mma_ss<KIND>(tmem + C::S_COL, sdesc_sw128(sQ + off, 16, 1024),
+                         sdesc_sw128(sK + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(B_SFULL));
+          mma_commit(bar(B_KFULL + 5 * ST + s));  // K stage free for the producer
+          if (j == it.nkv - 1) mma_commit(bar(B_QEMPTY));
         }
-        mma_commit(bar(B_SFULL));
-        mma_commit(bar(B_KFULL + 5 * ST + s));  // K stage free for the producer
-        if (j == it.nkv - 1) mma_commit(bar(B_QEMPTY));
+        __syncwarp();
         return true;
       };
       FwdItem cur = first;
       int k = 0, g = 0;
-      bool ok = mbar_wait(bar(qbar), 0, abort, 4, status) && issue_s(0, cur, 0);
+      bool ok = mbar_wait_warp(bar(qbar), 0, abort, 4, status) && issue_s(0, cur, 0);
       while (ok) {
         FwdItem nx;
         const bool has_next = k + 1 < kMaxItems && fwd_item(a, T, k + 1, nx);
@@ -287,7 +292,7 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
           // after this tile's P V, so that the Q load does not hold it up.
           bool s_late = false;
           if (j + 1 < cur.nkv || has_next) {
-            if (!mbar_wait(bar(B_SFREE), g & 1, abort, 5, status)) {
+            if (!mbar_wait_warp(bar(B_SFREE), g & 1, abort, 5, status)) {
               ok = false;
               break;
             }
@@ -296,7 +301,7 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
                 ok = false;
                 break;
               }
-            } else if (mbar_test(bar(qbar), (k + 1) & 1)) {
+            } else if (mbar_test_warp(bar(qbar), (k + 1) & 1)) {
               if (!issue_s(g + 1, nx, 0)) {
                 ok = false;
                 break;
@@ -307,40 +312,44 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
           }
           // The item's first P V overwrites O: the previous epilogue must
           // have read it.
-          if (j == 0 && k > 0 && !mbar_wait(bar(B_OFREE), (k - 1) & 1, abort, 16, status)) {
+          if (j == 0 && k > 0 &&
+              !mbar_wait_warp(bar(B_OFREE), (k - 1) & 1, abort, 16, status)) {
             ok = false;
             break;
           }
           const int s = g % ST;
           const int vbar = C::TRANSPOSE_V ? B_KFULL + 3 * ST + s : B_KFULL + ST + s;
-          if (!mbar_wait(bar(vbar), (g / ST) & 1, abort, 7, status)) {
+          if (!mbar_wait_warp(bar(vbar), (g / ST) & 1, abort, 7, status)) {
             ok = false;
             break;
           }
           const uint32_t sV = sKV + (2 * s + 1) * C::TILE_BYTES;
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
-            if (!mbar_wait(bar(hf == 0 ? B_PFULL1 : B_PFULL2), g & 1, abort, 6, status)) {
+            if (!mbar_wait_warp(bar(hf == 0 ? B_PFULL1 : B_PFULL2), g & 1, abort, 6, status)) {
               ok = false;
               break;
             }
             tc_fence_after();
+            if (elect_one()) {
 #pragma unroll
-            for (int kk = hf * C::NK_PV / 2; kk < (hf + 1) * C::NK_PV / 2; ++kk) {
-              uint64_t bdesc;
-              if constexpr (C::TRANSPOSE_V)  // V^T K-major: 32-B K-step, 4 per 128-B block
-                bdesc = sdesc_sw128(
-                    sVT + s * C::VT_BYTES + (kk / 4) * C::VT_BLK_BYTES + (kk % 4) * 32, 16, 1024);
-              else  // V MN-major: K-step = KPER rows of 128 B
-                bdesc = sdesc_sw128(sV + kk * C::KPER * 128, C::BLK_BYTES, 1024);
-              mma_ts<KIND>(tmem + C::O_COL, tmem + C::P_COL + kk * 8, bdesc, idPV,
-                           (j > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = hf * C::NK_PV / 2; kk < (hf + 1) * C::NK_PV / 2; ++kk) {
+                uint64_t bdesc;
+                if constexpr (C::TRANSPOSE_V)  // V^T K-major: 32-B K-step, 4 per 128-B block
+                  bdesc = sdesc_sw128(
+                      sVT + s * C::VT_BYTES + (kk / 4) * C::VT_BLK_BYTES + (kk % 4) * 32, 16, 1024);
+                else  // V MN-major: K-step = KPER rows of 128 B
+                  bdesc = sdesc_sw128(sV + kk * C::KPER * 128, C::BLK_BYTES, 1024);
+                mma_ts<KIND>(tmem + C::O_COL, tmem + C::P_COL + kk * 8, bdesc, idPV,
+                             (j > 0 || kk > 0) ? 1u : 0u);
+              }
+              if (hf == 1) mma_commit(bar(B_KFULL + 2 * ST + s));  // V stage free for the producer
+              mma_commit(bar(hf == 0 ? B_ODONE1 : B_ODONE2));
             }
-            if (hf == 1) mma_commit(bar(B_KFULL + 2 * ST + s));  // V stage free for the producer
-            mma_commit(bar(hf == 0 ? B_ODONE1 : B_ODONE2));
+            __syncwarp();
           }
           if (!ok) break;
-          if (s_late && (!mbar_wait(bar(qbar), (k + 1) & 1, abort, 4, status) ||
+          if (s_late && (!mbar_wait_warp(bar(qbar), (k + 1) & 1, abort, 4, status) ||
                          !issue_s(g + 1, nx, 0))) {
             ok = false;
             break;
@@ -350,8 +359,9 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
         cur = nx;
         ++k;
       }
-      // Everything this thread issued must finish before TMEM is freed.
-      mma_commit(bar(B_DRAIN));
+      // Everything this warp issued must finish before TMEM is freed.
+      if (elect_one()) mma_commit(bar(B_DRAIN));
+      __syncwarp();
       mbar_wait_drain(bar(B_DRAIN), 0, 8, status);
     }
   } else if (warp >= 6) {

@@ -152,8 +152,8 @@ WsLayout ws_layout(int B, int H, int Hkv, int N, int d, int dtype) {
   if (dtype == NEA_BF16) {
     w.dqacc = end;
     end += align256(rows * d * sizeof(float));
-    w.fold = end;  // 2 tiles x 128 rows x 16 bf16 per 128-row query tile
-    end += align256(prows / kTile * 8192);
+    w.fold = end;  // 2 tiles x 128 rows x 8 bf16 per 128-row query tile
+    end += align256(prows / kTile * 4096);
   } else {
     w.qt = end;
     w.dot = w.qt + align256(prows * d * sizeof(float));
@@ -288,7 +288,7 @@ int nea_attn_bwd_preprocess(const void* O, const void* dO, const float* LSE, voi
   int st = prepare_bwd(&a, nullptr, nullptr, nullptr, O, dO, LSE, dQ, nullptr, nullptr, workspace,
                        workspace_bytes, B, H, Hkv, N, d, scale, 1, dtype, true, false, false);
   if (st != NEA_OK) return st;
-  return launch_bwd_pre(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? NEA_OK
+  return launch_bwd_pre(a, sm_count(), static_cast<cudaStream_t>(stream)) == cudaSuccess ? NEA_OK
                                                                              : NEA_ERR_CUDA;
 }
 
@@ -310,7 +310,7 @@ int nea_attn_bwd_finalize(void* dQ, void* workspace, size_t workspace_bytes, int
                        false, false, false);
   if (st != NEA_OK) return st;
   if (dtype != NEA_BF16) return NEA_OK;
-  return launch_bwd_post(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? NEA_OK
+  return launch_bwd_post(a, sm_count(), static_cast<cudaStream_t>(stream)) == cudaSuccess ? NEA_OK
                                                                               : NEA_ERR_CUDA;
 }
 
@@ -323,10 +323,10 @@ int nea_attn_bwd(const void* Q, const void* K, const void* V, const void* O, con
                        N, d, scale, causal, dtype, true, true, true);
   if (st != NEA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (launch_bwd_pre(a, s) != cudaSuccess) return NEA_ERR_CUDA;
+  if (launch_bwd_pre(a, sm_count(), s) != cudaSuccess) return NEA_ERR_CUDA;
   st = run_main(a, s);
   if (st != NEA_OK) return st;
-  if (dtype == NEA_BF16 && launch_bwd_post(a, s) != cudaSuccess) return NEA_ERR_CUDA;
+  if (dtype == NEA_BF16 && launch_bwd_post(a, sm_count(), s) != cudaSuccess) return NEA_ERR_CUDA;
   return NEA_OK;
 }
 
@@ -372,16 +372,16 @@ int nea_attn_bwd_ex(const void* Q, const void* K, const void* V, const void* O, 
     // query tile; no accumulator to clear or cast
     a.deterministic = 1;
     a.dq_acc = nullptr;
-    if (launch_bwd_pre(a, s) != cudaSuccess || launch_bwd_main(a, s) != cudaSuccess ||
+    if (launch_bwd_pre(a, sm_count(), s) != cudaSuccess || launch_bwd_main(a, s) != cudaSuccess ||
         launch_bwd_dq(a, s) != cudaSuccess)
       return NEA_ERR_CUDA;
     return NEA_OK;
   }
   // fp32 already owns each dQ tile in one CTA, so it is deterministic as is
-  if (launch_bwd_pre(a, s) != cudaSuccess) return NEA_ERR_CUDA;
+  if (launch_bwd_pre(a, sm_count(), s) != cudaSuccess) return NEA_ERR_CUDA;
   st = run_main(a, s);
   if (st != NEA_OK) return st;
-  if (dtype == NEA_BF16 && launch_bwd_post(a, s) != cudaSuccess) return NEA_ERR_CUDA;
+  if (dtype == NEA_BF16 && launch_bwd_post(a, sm_count(), s) != cudaSuccess) return NEA_ERR_CUDA;
   return NEA_OK;
 }
 

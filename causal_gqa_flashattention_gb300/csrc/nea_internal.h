@@ -31,7 +31,7 @@ struct BwdArgs {
   float* delta;                     // workspace: D [B*H*N]
   float* lse2;                      // workspace: -LSE * log2(e) [B*H*N]
   float* dq_acc;                    // bf16: fp32 dQ accumulator [B,H,N,d]; fp32: null
-  uint16_t* fold;                   // bf16: per (head, 128-row query tile) two 128 x 16
+  uint16_t* fold;                   // bf16: per (head, 128-row query tile) two 128 x 8
                                     // bf16 tiles of row terms for the main kernel's MMAs
                                     // (-LSE/scale, -D as hi/mid/lo parts); fp32: null
   float* qt;                        // fp32 only: tf32-rounded Q^T  [B*H][d][N]
@@ -75,9 +75,10 @@ int decode_chunk_rows();
 // cudaError_t of its launch(es).
 // bf16: a persistent wave of min(items, sms x CTAs per SM) CTAs; tf32: one CTA per item.
 cudaError_t launch_fwd(const FwdArgs& a, int sms, cudaStream_t stream);
-cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t stream);
+// The HBM-bound preprocess and cast run one wave of blocks over `sms` SMs.
+cudaError_t launch_bwd_pre(const BwdArgs& a, int sms, cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream);
-cudaError_t launch_bwd_post(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_post(const BwdArgs& a, int sms, cudaStream_t stream);
 // Deterministic bf16 dQ: one CTA per query tile walks its key tiles in order.
 cudaError_t launch_bwd_dq(const BwdArgs& a, cudaStream_t stream);
 // fp32 path: transposes for the workspace, then the dK/dV and dQ kernels.

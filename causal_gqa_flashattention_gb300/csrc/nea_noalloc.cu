@@ -18,7 +18,7 @@ namespace {
 
 // The layout nea_attn_bwd_workspace_bytes() describes, each part rounded up
 // to 256 bytes (padded rows: N rounded up to a multiple of 128 per head).
-// 32 MiB covers, e.g., B*H*N = 98304 rows at d = 64 bf16 (30.8 MB).
+// 32 MiB covers, e.g., B*H*N = 98304 rows at d = 64 bf16 (27.7 MB).
 constexpr size_t kScratchBytes = size_t(32) << 20;
 constexpr int kMaxDevices = 64;
 

@@ -145,6 +145,23 @@ __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bo
   return r != 0;
 }
 
+// One lane of a converged warp (elect.sync).  Issuing tcgen05.mma / commit
+// from the elected lane of a converged warp keeps the issue stream fast;
+// the same instructions under a divergent branch (a loop that only lane 0
+// runs) advance far more slowly.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+// Warp-uniform form of mbar_test: lane 0's answer, broadcast.
+__device__ __forceinline__ bool mbar_test_warp(uint32_t bar, uint32_t parity) {
+  return __shfl_sync(0xffffffffu, mbar_test(bar, parity) ? 1 : 0, 0) != 0;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
@@ -289,14 +306,14 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
 }
 
 // Shared-memory matrix descriptor without swizzle, K-major, for a K = 16
-// bf16 operand: 8-row x 16-B core matrices, each 128 contiguous bytes; the
-// two core matrices of a row group (K elements 0-7, 8-15) lie LBO = 128 B
-// apart and row groups SBO = 256 B apart (a 128-row operand is 4 KB).
+// bf16 operand of 128 rows: 8-row x 16-B core matrices, each 128 contiguous
+// bytes.  K elements 0-7 of all rows come first (row r at r * 16: row groups
+// SBO = 128 B apart), K elements 8-15 LBO = 2 KB further on (a 4 KB operand).
 __device__ __forceinline__ uint64_t sdesc_k16(uint32_t saddr) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-  d |= static_cast<uint64_t>(128u >> 4) << 16;
-  d |= static_cast<uint64_t>(256u >> 4) << 32;
+  d |= static_cast<uint64_t>(2048u >> 4) << 16;
+  d |= static_cast<uint64_t>(128u >> 4) << 32;
   d |= 1ull << 46;
   return d;
 }

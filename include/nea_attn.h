@@ -76,8 +76,8 @@ int nea_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LS
  * Bytes of device workspace nea_attn_bwd() needs for these sizes (256-byte
  * aligned sub-buffers, with Npad = N rounded up to a multiple of 128:
  * D [B*H][Npad] fp32, -LSE*log2(e) [B*H][Npad] fp32, then for bf16 the fp32
- * dQ accumulator [B,H,N,d] and two 4 KB row-term tiles per 128-row query
- * tile [B*H][Npad/128][2][4096 B], for fp32 the transposed operands Q^T,
+ * dQ accumulator [B,H,N,d] and two 2 KB row-term tiles per 128-row query
+ * tile [B*H][Npad/128][2][2048 B], for fp32 the transposed operands Q^T,
  * dO^T [B*H][d][Npad] and K^T [B*Hkv][d][Npad]).  Returns 0 for invalid or
  * unsupported sizes.
  */
@@ -146,12 +146,12 @@ int nea_attn_bwd_finalize(void* dQ, void* workspace, size_t workspace_bytes, int
  * allowed.  Same arguments and results as nea_attn_bwd() minus the
  * workspace; the scratch it needs (the layout nea_attn_bwd_workspace_bytes()
  * describes: for bf16 D, -LSE*log2(e), the fp32 dQ accumulator and the
- * row-term tiles of the main kernel, about 4*d + 72 bytes per query row;
+ * row-term tiles of the main kernel, about 4*d + 40 bytes per query row;
  * for fp32 D, -LSE*log2(e) and the transposed Q, dO and K, about
  * 4*(2d+2) bytes per query row plus 4*d per key row) lives in a fixed
  * array of nea_attn_bwd_noalloc_max_bytes() bytes (32 MiB) inside the
- * library.  So bf16 takes up to about 102,000 query rows (B*H*N) at
- * d = 64 (the GPT-2-small shape, 98,304 rows, fits) and 57,000 at d = 128;
+ * library.  So bf16 takes up to about 113,000 query rows (B*H*N) at
+ * d = 64 (the GPT-2-small shape, 98,304 rows, fits) and 60,000 at d = 128;
  * fp32 at d = 64 about 43,000 (H = Hkv) to 55,000 (H = 3 Hkv).
  *   - Sizes whose nea_attn_bwd_workspace_bytes() exceeds that maximum return
  *     NEA_ERR_WORKSPACE and launch nothing.

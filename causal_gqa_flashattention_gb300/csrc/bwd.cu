@@ -850,7 +850,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
     const int quad = warp & 3;
     const int qr = quad * 32 + lane;  // query row == TMEM lane of the dQ tile
     const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    const bool leader = warp == C::DQ_WARP0 && lane == 0;
+    const bool lead_warp = warp == C::DQ_WARP0;  // its elected lane issues the reductions
     Tracer tr(NEA_TRACE_BASE, traced && warp == C::DQ_WARP0, 6);
     for (int n = 0; n < nsteps; ++n) {
       int h, i;
@@ -877,7 +877,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
         for (int box = 0; box < 2; ++box) {
           const uint32_t(&v)[32] = box == 0 ? v0 : v1;
           // the staging buffer is free once the previous reduction has read it
-          if (leader) bulk_wait_read0();
+          if (lead_warp) {
+            if (elect_one()) bulk_wait_read0();
+            __syncwarp();
+          }
           named_bar_sync(2, 128);
           uint8_t* rowp = smem + C::OFF_DQ + qr * 128;
 #pragma unroll
@@ -886,15 +889,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
                 make_uint4(v[4 * ch], v[4 * ch + 1], v[4 * ch + 2], v[4 * ch + 3]);
           fence_proxy_async();
           named_bar_sync(2, 128);
-          if (leader) {
-            tma_reduce_add_3d(&a.tmdQacc, sDQ, 64 * pr + 32 * box, i * kTile, bh);
-            bulk_commit();
+          if (lead_warp) {
+            if (elect_one()) {
+              tma_reduce_add_3d(&a.tmdQacc, sDQ, 64 * pr + 32 * box, i * kTile, bh);
+              bulk_commit();
+            }
+            __syncwarp();
           }
         }
       }
       tr.ev(42);
     }
-    if (leader) bulk_wait0();
+    if (lead_warp) {
+      if (elect_one()) bulk_wait0();
+      __syncwarp();
+    }
   }
   tc_fence_before();
   __syncthreads();

@@ -172,7 +172,8 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // converged warp, warp-uniform waits; one elected lane issues the copies
+    {
       // K runs one tile ahead of V: K_g is read by S_g, which is issued
       // before O += P_{g-1} V_{g-1}; V_g only by P_g V_g.  A stage of K is
       // refilled once the S that read it is done, a stage of V once its P V
@@ -201,41 +202,50 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
         if (!v_due) {
           if (ck.j == 0) {
             // Q's buffer is free once the previous item's S MMAs are done.
-            if (ck.k > 0 && !mbar_wait(bar(B_QEMPTY), (ck.k - 1) & 1, abort, 15, status)) {
+            if (ck.k > 0 && !mbar_wait_warp(bar(B_QEMPTY), (ck.k - 1) & 1, abort, 15, status)) {
               ok = false;
               break;
             }
-            mbar_expect_tx(bar(B_QFULL), C::TILE_BYTES);
-            for (int kb = 0; kb < C::NBLK; ++kb)
-              tma_load_3d(sQ + kb * C::BLK_BYTES, &a.tmQ, bar(B_QFULL), kb * C::BLK_ELEMS,
-                          ck.it.qt * kTile, ck.it.bh);
+            if (elect_one()) {
+              mbar_expect_tx(bar(B_QFULL), C::TILE_BYTES);
+              for (int kb = 0; kb < C::NBLK; ++kb)
+                tma_load_3d(sQ + kb * C::BLK_BYTES, &a.tmQ, bar(B_QFULL), kb * C::BLK_ELEMS,
+                            ck.it.qt * kTile, ck.it.bh);
+            }
+            __syncwarp();
             qloads = ck.k + 1;
           }
           const int s = gk % ST;
           if (gk >= ST &&
-              !mbar_wait(bar(B_KFULL + 5 * ST + s), ((gk / ST) - 1) & 1, abort, 1, status)) {
+              !mbar_wait_warp(bar(B_KFULL + 5 * ST + s), ((gk / ST) - 1) & 1, abort, 1, status)) {
             ok = false;
             break;
           }
           const uint32_t sK = sKV + (2 * s) * C::TILE_BYTES;
-          mbar_expect_tx(bar(B_KFULL + s), C::TILE_BYTES);
-          for (int kb = 0; kb < C::NBLK; ++kb)
-            tma_load_3d(sK + kb * C::BLK_BYTES, &a.tmK, bar(B_KFULL + s), kb * C::BLK_ELEMS,
-                        ck.j * kTile, kv_head(ck.it));
+          if (elect_one()) {
+            mbar_expect_tx(bar(B_KFULL + s), C::TILE_BYTES);
+            for (int kb = 0; kb < C::NBLK; ++kb)
+              tma_load_3d(sK + kb * C::BLK_BYTES, &a.tmK, bar(B_KFULL + s), kb * C::BLK_ELEMS,
+                          ck.j * kTile, kv_head(ck.it));
+          }
+          __syncwarp();
           ++gk;
           advance(ck);
         } else {
           const int s = gv % ST;
           if (gv >= ST &&
-              !mbar_wait(bar(B_KFULL + 2 * ST + s), ((gv / ST) - 1) & 1, abort, 17, status)) {
+              !mbar_wait_warp(bar(B_KFULL + 2 * ST + s), ((gv / ST) - 1) & 1, abort, 17, status)) {
             ok = false;
             break;
           }
           const uint32_t sV = sKV + (2 * s + 1) * C::TILE_BYTES;
-          mbar_expect_tx(bar(B_KFULL + ST + s), C::TILE_BYTES);
-          for (int kb = 0; kb < C::NBLK; ++kb)
-            tma_load_3d(sV + kb * C::BLK_BYTES, &a.tmV, bar(B_KFULL + ST + s), kb * C::BLK_ELEMS,
-                        cv.j * kTile, kv_head(cv.it));
+          if (elect_one()) {
+            mbar_expect_tx(bar(B_KFULL + ST + s), C::TILE_BYTES);
+            for (int kb = 0; kb < C::NBLK; ++kb)
+              tma_load_3d(sV + kb * C::BLK_BYTES, &a.tmV, bar(B_KFULL + ST + s),
+                          kb * C::BLK_ELEMS, cv.j * kTile, kv_head(cv.it));
+          }
+          __syncwarp();
           ++gv;
           advance(cv);
         }
@@ -569,7 +579,10 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
       // ------------------------------------------------------------ epilogue
       if (ok) ok = mbar_wait_warp(bar(B_ODONE2), (g - 1) & 1, abort, 11, status);
       if (k > 0) {  // the previous item's store must have read the staging buffer
-        if (warp == 2 && lane == 0) bulk_wait_read0();
+        if (warp == 2) {
+          if (elect_one()) bulk_wait_read0();
+          __syncwarp();
+        }
         named_bar_sync(1, 128);
       }
       if (ok) {
@@ -615,13 +628,19 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
         fence_proxy_async();
       }
       named_bar_sync(1, 128);
-      if (warp == 2 && lane == 0 && !*abort) {
-        for (int kb = 0; kb < C::NBLK; ++kb)
-          tma_store_3d(&a.tmO, sO + kb * C::BLK_BYTES, kb * C::BLK_ELEMS, it.qt * kTile, it.bh);
-        bulk_commit();
+      if (warp == 2) {
+        if (elect_one() && !*abort) {
+          for (int kb = 0; kb < C::NBLK; ++kb)
+            tma_store_3d(&a.tmO, sO + kb * C::BLK_BYTES, kb * C::BLK_ELEMS, it.qt * kTile, it.bh);
+          bulk_commit();
+        }
+        __syncwarp();
       }
     }  // items
-    if (warp == 2 && lane == 0) bulk_wait0();
+    if (warp == 2) {
+      if (elect_one()) bulk_wait0();
+      __syncwarp();
+    }
   }
   tc_fence_before();
   __syncthreads();

@@ -64,6 +64,20 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     return LIB
 
 
+def build_variant(name: str, flags) -> str:
+    """Build the library with extra nvcc flags into _build/<name>/ (a separate
+    copy used by tests, e.g. the build whose bounded waits run out quickly);
+    returns its path.  The default library is not touched."""
+    global LIB, OBJDIR
+    saved = LIB, OBJDIR
+    try:
+        OBJDIR = os.path.join(HERE, "_build", name)
+        LIB = os.path.join(OBJDIR, "libnea_attn.so")
+        return build(force=True, extra_flags=tuple(flags))
+    finally:
+        LIB, OBJDIR = saved
+
+
 if __name__ == "__main__":
     build(force="--force" in sys.argv, verbose="-v" in sys.argv)
     print(LIB)

@@ -72,10 +72,59 @@ unsigned int* status_ptr() {
   return g_status_ptr[dev];
 }
 
+// Encoded tensor maps, reused across calls: a map depends only on the base
+// address, element type and shape, so a repeated call on the same buffers
+// skips the driver's encode.  Small and least-recently-used.
+struct MapKey {
+  const void* base;
+  long long heads;
+  int dt, esize, d, N, transposed;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && heads == o.heads && dt == o.dt && esize == o.esize && d == o.d &&
+           N == o.N && transposed == o.transposed;
+  }
+};
+constexpr int kMapCache = 64;
+struct MapEntry {
+  MapKey key;
+  CUtensorMap map;
+  unsigned long long used;  // 0: empty
+};
+std::mutex g_map_mu;
+MapEntry g_maps[kMapCache];
+unsigned long long g_map_clock = 0;
+
+bool map_lookup(const MapKey& k, CUtensorMap* m) {
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  for (MapEntry& e : g_maps)
+    if (e.used != 0 && e.key == k) {
+      e.used = ++g_map_clock;
+      *m = e.map;
+      return true;
+    }
+  return false;
+}
+void map_store(const MapKey& k, const CUtensorMap& m) {
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  MapEntry* victim = &g_maps[0];
+  for (MapEntry& e : g_maps) {
+    if (e.used == 0) {
+      victim = &e;
+      break;
+    }
+    if (e.used < victim->used) victim = &e;
+  }
+  victim->key = k;
+  victim->map = m;
+  victim->used = ++g_map_clock;
+}
+
 // 3-D view {d, N, heads} of a [heads][N][d] array, boxes of 128 B x 128 rows
 // with 128-byte swizzle (the layout the tensor-core descriptors expect).
 bool encode_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, int d, int N,
                long long heads) {
+  const MapKey key{base, heads, static_cast<int>(dt), esize, d, N, 0};
+  if (map_lookup(key, m)) return true;
   EncodeTiledFn enc = encoder();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
@@ -84,15 +133,19 @@ bool encode_3d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esi
                            static_cast<cuuint64_t>(d) * esize * static_cast<cuuint64_t>(N)};
   cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esize), static_cast<cuuint32_t>(kTile), 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-         CUDA_SUCCESS;
+  if (enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  map_store(key, *m);
+  return true;
 }
 
 // 3-D view {N, d, heads} of a transposed fp32 [heads][d][N] array: boxes of
 // 32 columns (128 B) x d rows, 128-byte swizzle (K-major tf32 operands).
 bool encode_3d_t(CUtensorMap* m, const void* base, int d, int N, long long heads) {
+  const MapKey key{base, heads, static_cast<int>(CU_TENSOR_MAP_DATA_TYPE_FLOAT32), 4, d, N, 1};
+  if (map_lookup(key, m)) return true;
   EncodeTiledFn enc = encoder();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(d),
@@ -101,9 +154,12 @@ bool encode_3d_t(CUtensorMap* m, const void* base, int d, int N, long long heads
                            static_cast<cuuint64_t>(N) * 4 * static_cast<cuuint64_t>(d)};
   cuuint32_t box[3] = {32, static_cast<cuuint32_t>(d), 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box,
+          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  map_store(key, *m);
+  return true;
 }
 
 bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

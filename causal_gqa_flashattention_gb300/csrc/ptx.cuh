@@ -19,6 +19,17 @@ constexpr unsigned int kStatusTimeout = 1u;
 
 // A wait gives up after this many SM clock cycles (about 2 s at 2 GHz).
 constexpr long long kWaitCycles = 4000000000LL;
+// The limit of the abortable waits.  A test build (-DNEA_WAIT_TEST=<cycles>)
+// lowers it and checks it without suspending in the wait instruction, so
+// that ordinary waits run out and the kernels' unwind paths run; the waits
+// that drain a CTA's own copies and MMAs before it exits keep kWaitCycles.
+#ifdef NEA_WAIT_TEST
+constexpr long long kWaitLimit = NEA_WAIT_TEST;
+constexpr bool kWaitSleep = false;
+#else
+constexpr long long kWaitLimit = kWaitCycles;
+constexpr bool kWaitSleep = true;
+#endif
 // Between checks of the abort flag and the clock, a waiting thread sleeps in
 // mbarrier.try_wait for at most this long; the hardware wakes it as soon as
 // the phase completes.  Spinning instead (try_wait without a hint, a
@@ -80,16 +91,19 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed.  Gives up when
-// another role of the CTA raised *abort, or after kWaitCycles; in the latter
-// case it raises *abort itself and records `id` in *status.
+// another role of the CTA raised *abort, or after kWaitLimit cycles; in the
+// latter case it raises *abort itself and records `id` in *status.
+// (mbarrier.try_wait may itself block until the phase completes; the test
+// build polls with test_wait instead, so that its short limit can run out.)
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           uint32_t id, unsigned int* status) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (kWaitSleep ? mbar_try_wait(bar, parity) : mbar_test(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait_sleep(bar, parity, kSuspendNs)) return true;
+    if (kWaitSleep ? mbar_try_wait_sleep(bar, parity, kSuspendNs) : mbar_test(bar, parity))
+      return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > kWaitLimit) {
       *abort = 1;
       atomicOr(status, kStatusTimeout | ((id & 0xffu) << 8));
       return false;

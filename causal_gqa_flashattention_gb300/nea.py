@@ -48,42 +48,57 @@ def lib():
             if not os.path.exists(LIB_PATH):
                 raise RuntimeError(f"{LIB_PATH} is missing: build it with "
                                    "`python -c 'import __graft_entry__ as g; g.build()'`")
-            L = ctypes.CDLL(LIB_PATH)
-            L.nea_attn_fwd.argtypes = [_vp] * 5 + [_i] * 5 + [_f, _i, _i, _vp]
-            L.nea_attn_fwd.restype = _i
-            L.nea_attn_bwd_workspace_bytes.argtypes = [_i] * 6
-            L.nea_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
-            L.nea_attn_bwd.argtypes = [_vp] * 10 + [ctypes.c_size_t] + [_i] * 5 + [_f, _i, _i, _vp]
-            L.nea_attn_bwd.restype = _i
-            L.nea_attn_bwd_preprocess.argtypes = [_vp] * 5 + [ctypes.c_size_t] + [_i] * 5 + [
-                _f, _i, _vp]
-            L.nea_attn_bwd_preprocess.restype = _i
-            L.nea_attn_bwd_main.argtypes = [_vp] * 8 + [ctypes.c_size_t] + [_i] * 5 + [
-                _f, _i, _i, _vp]
-            L.nea_attn_bwd_main.restype = _i
-            L.nea_attn_bwd_finalize.argtypes = [_vp] * 2 + [ctypes.c_size_t] + [_i] * 6 + [_vp]
-            L.nea_attn_bwd_finalize.restype = _i
-            L.nea_rope_table.argtypes = [_vp, _i, _i, ctypes.c_double, _vp]
-            L.nea_rope_table.restype = _i
-            L.nea_rope_qk.argtypes = [_vp] * 5 + [_i] * 6 + [_vp]
-            L.nea_rope_qk.restype = _i
-            L.nea_attn_bwd_rope.argtypes = [_vp] * 11 + [ctypes.c_size_t] + [_i] * 5 + [
-                _f, _i, _i, _vp]
-            L.nea_attn_bwd_rope.restype = _i
-            L.nea_attn_bwd_ex.argtypes = [_vp] * 7 + [_i] + [_vp] * 4 + [ctypes.c_size_t] + [
-                _i] * 5 + [_f, _i, _i, _vp]
-            L.nea_attn_bwd_ex.restype = _i
-            L.nea_attn_decode_workspace_bytes.argtypes = [_i] * 6
-            L.nea_attn_decode_workspace_bytes.restype = ctypes.c_size_t
-            L.nea_attn_decode.argtypes = [_vp] * 7 + [ctypes.c_size_t] + [_i] * 6 + [_f, _i, _vp]
-            L.nea_attn_decode.restype = _i
-            L.nea_attn_check_status.argtypes = [_vp]
-            L.nea_attn_check_status.restype = _i
-            L.nea_status_string.argtypes = [_i]
-            L.nea_status_string.restype = ctypes.c_char_p
-            L.nea_version.restype = _i
-            _lib = L
+            _lib = load_library(LIB_PATH)
     return _lib
+
+
+def load_library(path):
+    """Load a build of the library from ``path`` and declare its C ABI."""
+    L = ctypes.CDLL(path)
+    L.nea_attn_fwd.argtypes = [_vp] * 5 + [_i] * 5 + [_f, _i, _i, _vp]
+    L.nea_attn_fwd.restype = _i
+    L.nea_attn_bwd_workspace_bytes.argtypes = [_i] * 6
+    L.nea_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+    L.nea_attn_bwd.argtypes = [_vp] * 10 + [ctypes.c_size_t] + [_i] * 5 + [_f, _i, _i, _vp]
+    L.nea_attn_bwd.restype = _i
+    L.nea_attn_bwd_preprocess.argtypes = [_vp] * 5 + [ctypes.c_size_t] + [_i] * 5 + [
+        _f, _i, _vp]
+    L.nea_attn_bwd_preprocess.restype = _i
+    L.nea_attn_bwd_main.argtypes = [_vp] * 8 + [ctypes.c_size_t] + [_i] * 5 + [
+        _f, _i, _i, _vp]
+    L.nea_attn_bwd_main.restype = _i
+    L.nea_attn_bwd_finalize.argtypes = [_vp] * 2 + [ctypes.c_size_t] + [_i] * 6 + [_vp]
+    L.nea_attn_bwd_finalize.restype = _i
+    L.nea_rope_table.argtypes = [_vp, _i, _i, ctypes.c_double, _vp]
+    L.nea_rope_table.restype = _i
+    L.nea_rope_qk.argtypes = [_vp] * 5 + [_i] * 6 + [_vp]
+    L.nea_rope_qk.restype = _i
+    L.nea_attn_bwd_rope.argtypes = [_vp] * 11 + [ctypes.c_size_t] + [_i] * 5 + [
+        _f, _i, _i, _vp]
+    L.nea_attn_bwd_rope.restype = _i
+    L.nea_attn_bwd_ex.argtypes = [_vp] * 7 + [_i] + [_vp] * 4 + [ctypes.c_size_t] + [
+        _i] * 5 + [_f, _i, _i, _vp]
+    L.nea_attn_bwd_ex.restype = _i
+    L.nea_attn_decode_workspace_bytes.argtypes = [_i] * 6
+    L.nea_attn_decode_workspace_bytes.restype = ctypes.c_size_t
+    L.nea_attn_decode.argtypes = [_vp] * 7 + [ctypes.c_size_t] + [_i] * 6 + [_f, _i, _vp]
+    L.nea_attn_decode.restype = _i
+    L.nea_attn_check_status.argtypes = [_vp]
+    L.nea_attn_check_status.restype = _i
+    L.nea_status_string.argtypes = [_i]
+    L.nea_status_string.restype = ctypes.c_char_p
+    L.nea_version.restype = _i
+    return L
+
+
+def use_library(L):
+    """Make the calls of this module go to the loaded library ``L`` (from
+    load_library, e.g. a test build); returns the one they used before."""
+    global _lib
+    prev = lib()
+    with _lock:
+        _lib = L
+    return prev
 
 
 def status_string(status: int) -> str:

@@ -30,6 +30,7 @@
 // P [128+d, ...).  Key tiles above the causal diagonal are never loaded.
 #include "nea_internal.h"
 #include "ptx.cuh"
+#include "trace.cuh"
 
 namespace nea {
 namespace {
@@ -101,6 +102,14 @@ enum : int { B_QFULL = 0, B_SFULL, B_SFREE, B_PFULL1, B_PFULL2, B_ODONE1, B_ODON
 // K_EMPTY[s] = B_KFULL + 5 ST + s.  K and V stages are freed separately: K_j
 // once S_j is done, V_j once P_j V_j is done.
 
+#ifdef NEA_TRACE
+// Timeline of CTA 0: rows 0 producer, 1 MMA issuer, 2 first softmax warp.
+__device__ long long g_trace_fwd[kTraceRoles * kTraceEvents];
+#define NEA_TRACE_FWD g_trace_fwd
+#else
+#define NEA_TRACE_FWD nullptr
+#endif
+
 constexpr float kLog2e = 1.4426950408889634f;
 // Lazy rescale: O and l keep a stale row max until the true max exceeds it
 // by more than this (log2 units); P is then bounded by 2^8, exact in the end.
@@ -170,10 +179,12 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
 
+  const bool traced = blockIdx.x == 0 && lane == 0;
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // converged warp, warp-uniform waits; one elected lane issues the copies
     {
+      Tracer tr(NEA_TRACE_FWD, traced, 0);
       // K runs one tile ahead of V: K_g is read by S_g, which is issued
       // before O += P_{g-1} V_{g-1}; V_g only by P_g V_g.  A stage of K is
       // refilled once the S that read it is done, a stage of V once its P V
@@ -229,6 +240,7 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
                           ck.j * kTile, kv_head(ck.it));
           }
           __syncwarp();
+          tr.ev(1);
           ++gk;
           advance(ck);
         } else {
@@ -246,6 +258,7 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
                           kb * C::BLK_ELEMS, cv.j * kTile, kv_head(cv.it));
           }
           __syncwarp();
+          tr.ev(2);
           ++gv;
           advance(cv);
         }
@@ -264,6 +277,7 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
     // The whole warp runs the issue loop (waits are warp-uniform); one
     // elected lane issues each burst of MMAs and its commits.
     {
+      Tracer tr(NEA_TRACE_FWD, traced, 1);
       constexpr uint32_t idS = make_idesc<KIND>(128, 128, false, false);
       constexpr uint32_t idPV = make_idesc<KIND>(128, D, false, !C::TRANSPOSE_V);
       const int qbar = C::TRANSPOSE_V ? B_QREADY : B_QFULL;
@@ -273,6 +287,7 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
         const int s = g % ST;
         const int kbar = C::TRANSPOSE_V ? B_KFULL + 4 * ST + s : B_KFULL + s;
         if (!mbar_wait_warp(bar(kbar), (g / ST) & 1, abort, 3, status)) return false;
+        tr.ev(10);
         tc_fence_after();
         const uint32_t sK = sKV + (2 * s) * C::TILE_BYTES;
         if (elect_one()) {
@@ -287,6 +302,7 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
           if (j == it.nkv - 1) mma_commit(bar(B_QEMPTY));
         }
         __syncwarp();
+        tr.ev(11);
         return true;
       };
       FwdItem cur = first;
@@ -306,6 +322,7 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
               ok = false;
               break;
             }
+            tr.ev(12);
             if (j + 1 < cur.nkv) {
               if (!issue_s(g + 1, cur, j + 1)) {
                 ok = false;
@@ -340,6 +357,7 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
               ok = false;
               break;
             }
+            tr.ev(13 + 2 * hf);
             tc_fence_after();
             if (elect_one()) {
 #pragma unroll
@@ -357,6 +375,7 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
               mma_commit(bar(hf == 0 ? B_ODONE1 : B_ODONE2));
             }
             __syncwarp();
+            tr.ev(14 + 2 * hf);
           }
           if (!ok) break;
           if (s_late && (!mbar_wait_warp(bar(qbar), (k + 1) & 1, abort, 4, status) ||
@@ -446,6 +465,7 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
     const int r = quad * 32 + lane;  // row of the query tile == TMEM lane
     const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const float c = a.scale * kLog2e;
+    Tracer tr(NEA_TRACE_FWD, false, 2);  // (softmax events: off, the warps are at the register limit)
     // On an abort the warps keep walking the item list without waiting, so
     // that all four take part in the same named-barrier syncs.
     bool ok = true;
@@ -458,6 +478,7 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
           ok = false;
           break;
         }
+        tr.ev(30);
         tc_fence_after();
         uint32_t u0[32], u1[32], u2[32], u3[32];
         tmem_ld32(trow + C::S_COL + 0, u0);
@@ -470,6 +491,7 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
         reg_fence(u3);
         tc_fence_before();
         mbar_arrive(bar(B_SFREE));
+        tr.ev(31);
         float sv[128];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -509,6 +531,7 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
           m_ref = m_new;
         }
         const float moff = -m_ref * c;
+        tr.ev(32);
         // exponent arguments with packed fp32x2 FMAs; row sum in 4 packed chains
         const float2 c2 = make_float2(c, c), moff2 = make_float2(moff, moff);
         float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
@@ -570,6 +593,7 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive(bar(hf == 0 ? B_PFULL1 : B_PFULL2));
+          tr.ev(33 + hf);
         }
         if (!ok) break;
         const float2 r01 = __fadd2_rn(rs2[0], rs2[1]), r23 = __fadd2_rn(rs2[2], rs2[3]);
@@ -577,7 +601,9 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
         l = l * alpha + rs;
       }
       // ------------------------------------------------------------ epilogue
+      tr.ev(40);
       if (ok) ok = mbar_wait_warp(bar(B_ODONE2), (g - 1) & 1, abort, 11, status);
+      tr.ev(41);
       if (k > 0) {  // the previous item's store must have read the staging buffer
         if (warp == 2) {
           if (elect_one()) bulk_wait_read0();
@@ -676,3 +702,15 @@ cudaError_t launch_fwd(const FwdArgs& a, int sms, cudaStream_t stream) {
 }
 
 }  // namespace nea
+
+#ifdef NEA_TRACE
+// Copies the forward kernel's timeline to `host` (kTraceRoles * kTraceEvents
+// values, 0 where no event was recorded) and clears it for the next launch.
+extern "C" int nea_trace_read_fwd(long long* host) {
+  if (cudaMemcpyFromSymbol(host, nea::g_trace_fwd, sizeof(nea::g_trace_fwd)) != cudaSuccess)
+    return -1;
+  static long long zeros[nea::kTraceRoles * nea::kTraceEvents] = {};
+  return cudaMemcpyToSymbol(nea::g_trace_fwd, zeros, sizeof(zeros)) == cudaSuccess ? 0 : -1;
+}
+#endif
+

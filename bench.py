@@ -365,8 +365,24 @@ def run_cuda(args):
         if nea.check_status(stream) != nea.NEA_OK:
             raise RuntimeError("kernel status word set during the per-kernel timing")
     per = [[evs[i][s].elapsed_time(evs[i][s + 1]) for s in range(4)] for i in range(K)]
-    # per[i] = [fwd, bwd_pre, bwd_main, bwd_post] in ms
+    # per[i] = [fwd, bwd_pre, bwd_main, bwd_post] in ms, eager launches (the
+    # host work of each launch can land between the events)
     eager_ms = sum(sum(p) for p in per) / K
+    # each kernel alone, captured as a CUDA graph and replayed with L2
+    # flushed before each replay: device time without host-side gaps
+    stage_fns = [
+        lambda st: nea.attn_fwd(q, k, v, causal=True, scale=w.scale, out=o, lse=lse, stream=st),
+        lambda st: nea.attn_bwd_stages(q, k, v, o, do, lse, dq, dk, dv, wsp, causal=True,
+                                       scale=w.scale, stream=st, only={0}),
+        lambda st: nea.attn_bwd_stages(q, k, v, o, do, lse, dq, dk, dv, wsp, causal=True,
+                                       scale=w.scale, stream=st, only={1}),
+        lambda st: nea.attn_bwd_stages(q, k, v, o, do, lse, dq, dk, dv, wsp, causal=True,
+                                       scale=w.scale, stream=st, only={2}),
+    ]
+    alone = [_time_ms(fn, l2_flush, stream, K) for fn in (stage_fns if w.dtype == "bf16"
+                                                           else stage_fns[:3])]
+    if nea.check_status(stream) != nea.NEA_OK:
+        raise RuntimeError("kernel status word set during the per-kernel timing")
     if graph is not None:
         step_ms = [gev[i][0].elapsed_time(gev[i][1]) for i in range(K)]
     else:
@@ -374,6 +390,9 @@ def run_cuda(args):
     ms_step = max_over_ranks(sum(step_ms) / K, ws)
     flops = w.fwd_flops() + w.bwd_flops()
     value = job_value(flops, ms_step, ws)
+    # in-step per-kernel times (eager launches: each kernel finds in L2 what
+    # the previous one left there, as inside the step) for the table and the
+    # roofline; the isolated replays are reported beside them
     k_ms = [sum(p[s] for p in per) / K for s in range(4)]
     peaks, src = load_peaks()
     peak_tc = float(peaks["bf16_tflops"])
@@ -486,6 +505,11 @@ def run_cuda(args):
                    else "eager launches" + (f" (graph capture failed: {graph_error})"
                                             if not args.no_graph else "")),
         "eager_ms_per_step": round(eager_ms, 5),
+        "kernel_timing": "kernels: CUDA events between the step's kernels launched eagerly "
+                         "(each finds in L2 what the previous one left); kernels_alone_ms: "
+                         "each kernel alone as a CUDA graph replay, L2 flushed before each",
+        "kernels_alone_ms": {n: round(t, 5) for n, t in zip(("fwd", "bwd_pre", "bwd_main",
+                                                             "bwd_post"), alone)},
         "clocks": clk.summary(),
         "wall_s_timed_region": round(wall, 4),
     }
@@ -504,17 +528,34 @@ def run_cuda(args):
 
 
 def _time_ms(fn, l2_flush, stream, reps):
-    """Mean device time of fn() over reps calls, L2 flushed before each."""
+    """Mean device time of fn(st) over reps calls, L2 flushed before each.
+    The call is captured once as a CUDA graph and replayed, so that host-side
+    launch work does not land inside the events (eager launches if capture
+    fails)."""
     import torch
+    g = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+    except Exception:  # noqa: BLE001 - eager timing below
+        g = None
+
+    def run():
+        if g is not None:
+            g.replay()
+        else:
+            fn(stream)
     for _ in range(3):
         l2_flush()
-        fn()
+        run()
     ts = []
     for _ in range(reps):
         l2_flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        fn()
+        run()
         b.record(stream)
         b.synchronize()
         ts.append(a.elapsed_time(b))
@@ -531,17 +572,17 @@ def measure_extras(nea, w, q, k, v, do, o, lse, wsp, l2_flush, stream, peak_hbm,
     out = {}
     cs = nea.rope_table(w.N, w.d, device=q.device)
     qr, kr = torch.empty_like(q), torch.empty_like(k)
-    t_rot = _time_ms(lambda: nea.rope_qk(q, k, cs, qr=qr, kr=kr, stream=stream), l2_flush,
+    t_rot = _time_ms(lambda st: nea.rope_qk(q, k, cs, qr=qr, kr=kr, stream=st), l2_flush,
                      stream, reps)
     rot_bytes = 2 * (q.numel() + k.numel()) * q.element_size() + cs.numel() * 4
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    t_b = _time_ms(lambda: nea.attn_bwd(qr, kr, v, o, do, lse, dq=dq, dk=dk, dv=dv,
-                                        workspace=wsp, stream=stream), l2_flush, stream, reps)
-    t_br = _time_ms(lambda: nea.attn_bwd(qr, kr, v, o, do, lse, dq=dq, dk=dk, dv=dv,
-                                         workspace=wsp, stream=stream, rope_cs=cs),
+    t_b = _time_ms(lambda st: nea.attn_bwd(qr, kr, v, o, do, lse, dq=dq, dk=dk, dv=dv,
+                                           workspace=wsp, stream=st), l2_flush, stream, reps)
+    t_br = _time_ms(lambda st: nea.attn_bwd(qr, kr, v, o, do, lse, dq=dq, dk=dk, dv=dv,
+                                            workspace=wsp, stream=st, rope_cs=cs),
                     l2_flush, stream, reps)
-    t_det = _time_ms(lambda: nea.attn_bwd(qr, kr, v, o, do, lse, dq=dq, dk=dk, dv=dv,
-                                          workspace=wsp, stream=stream, deterministic=True),
+    t_det = _time_ms(lambda st: nea.attn_bwd(qr, kr, v, o, do, lse, dq=dq, dk=dk, dv=dv,
+                                             workspace=wsp, stream=st, deterministic=True),
                      l2_flush, stream, reps)
     out["bwd_deterministic"] = {"ms": round(t_det, 5), "ms_default": round(t_b, 5),
                                 "tflops": round(w.bwd_flops() / (t_det * 1e-3) / 1e12, 1),
@@ -555,10 +596,11 @@ def measure_extras(nea, w, q, k, v, do, o, lse, wsp, l2_flush, stream, peak_hbm,
                        "overhead_pct": round(100.0 * (t_br / t_b - 1.0), 2)}
     # full (non-causal) attention at the same shape: twice the causal work
     of, lf = torch.empty_like(o), torch.empty_like(lse)
-    t_ff = _time_ms(lambda: nea.attn_fwd(q, k, v, causal=False, out=of, lse=lf, stream=stream),
+    t_ff = _time_ms(lambda st: nea.attn_fwd(q, k, v, causal=False, out=of, lse=lf, stream=st),
                     l2_flush, stream, reps)
-    t_fb = _time_ms(lambda: nea.attn_bwd(q, k, v, of, do, lf, causal=False, dq=dq, dk=dk, dv=dv,
-                                         workspace=wsp, stream=stream), l2_flush, stream, reps)
+    t_fb = _time_ms(lambda st: nea.attn_bwd(q, k, v, of, do, lf, causal=False, dq=dq, dk=dk,
+                                            dv=dv, workspace=wsp, stream=st),
+                    l2_flush, stream, reps)
     full_flops = 2.0 * (w.fwd_flops() + w.bwd_flops())
     out["full_attention"] = {"fwd_ms": round(t_ff, 5), "bwd_ms": round(t_fb, 5),
                              "tflops": round(full_flops / ((t_ff + t_fb) * 1e-3) / 1e12, 1),
@@ -571,8 +613,8 @@ def measure_extras(nea, w, q, k, v, do, o, lse, wsp, l2_flush, stream, peak_hbm,
         wsd = torch.empty(max(nea.decode_workspace_bytes(dw.B, dw.H, dw.Hkv, dw.nq, dw.Lmax,
                                                           dw.d), 1),
                           dtype=torch.uint8, device=q.device)
-        t = _time_ms(lambda: nea.attn_decode(dq_, kc, vc, lens, out=od, lse=ld, workspace=wsd,
-                                             stream=stream), l2_flush, stream, reps)
+        t = _time_ms(lambda st: nea.attn_decode(dq_, kc, vc, lens, out=od, lse=ld,
+                                                workspace=wsd, stream=st), l2_flush, stream, reps)
         byt = dw.cache_bytes() + 2 * dq_.numel() * dq_.element_size() + ld.numel() * 4
         out[name] = {"ms": round(t, 5), "bytes": byt,
                      "gbs": round(byt / (t * 1e-3) / 1e9, 1),

@@ -220,34 +220,40 @@ def attn_bwd(q, k, v, o, do, lse, *, causal=True, scale=None, dq=None, dk=None, 
 
 
 def attn_bwd_stages(q, k, v, o, do, lse, dq, dk, dv, workspace, *, causal=True, scale=None,
-                    stream=None, between=None):
+                    stream=None, between=None, only=None):
     """The backward as its three ABI stages (same work as ``attn_bwd``).
     ``between(i)`` is called before stage i (0, 1, 2) and after the last
-    (i = 3), e.g. to record CUDA events between the kernels."""
+    (i = 3), e.g. to record CUDA events between the kernels.  ``only``: a set
+    of stage indices to run (default all), e.g. to time one stage alone on a
+    workspace that earlier calls have filled."""
     B, H, Hkv, N, d = _check(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     code = _dtype_code(q)
     s = ctypes.c_void_p(_stream_handle(stream))
     L = lib()
     nb = workspace.numel()
+    run = (lambda i: True) if only is None else (lambda i: i in only)
     if between:
         between(0)
-    st = L.nea_attn_bwd_preprocess(_ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(workspace), nb,
-                                   B, H, Hkv, N, d, scale, code, s)
-    if st != NEA_OK:
-        raise NeaError(st, "nea_attn_bwd_preprocess")
+    if run(0):
+        st = L.nea_attn_bwd_preprocess(_ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(workspace),
+                                       nb, B, H, Hkv, N, d, scale, code, s)
+        if st != NEA_OK:
+            raise NeaError(st, "nea_attn_bwd_preprocess")
     if between:
         between(1)
-    st = L.nea_attn_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
-                             _ptr(workspace), nb, B, H, Hkv, N, d, scale, int(bool(causal)), code,
-                             s)
-    if st != NEA_OK:
-        raise NeaError(st, "nea_attn_bwd_main")
+    if run(1):
+        st = L.nea_attn_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk),
+                                 _ptr(dv), _ptr(workspace), nb, B, H, Hkv, N, d, scale,
+                                 int(bool(causal)), code, s)
+        if st != NEA_OK:
+            raise NeaError(st, "nea_attn_bwd_main")
     if between:
         between(2)
-    st = L.nea_attn_bwd_finalize(_ptr(dq), _ptr(workspace), nb, B, H, Hkv, N, d, code, s)
-    if st != NEA_OK:
-        raise NeaError(st, "nea_attn_bwd_finalize")
+    if run(2):
+        st = L.nea_attn_bwd_finalize(_ptr(dq), _ptr(workspace), nb, B, H, Hkv, N, d, code, s)
+        if st != NEA_OK:
+            raise NeaError(st, "nea_attn_bwd_finalize")
     if between:
         between(3)
     return dq, dk, dv

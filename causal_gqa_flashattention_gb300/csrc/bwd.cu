@@ -242,13 +242,17 @@ struct BwdCfg {
   // group q owns query columns [32 q, 32 q + 32) of every step.
   static constexpr int NGRP = 4;
   static constexpr int NCW = 4 * NGRP;  // compute warps
-  // P^T as packed bf16: group q writes its 32 queries (16 columns) at
-  // P_COL + q * P_GSTRIDE.  d = 128 keeps them inside the group's own S^T
-  // columns, which it has already read.
-  static constexpr int P_COL = D == 64 ? 448 : 0;
-  static constexpr int P_GSTRIDE = D == 64 ? 16 : 32;
+  // P^T as packed bf16: group q writes its 32 queries (16 columns) inside
+  // its own S^T columns, which it has already read (P_COL + q * P_GSTRIDE).
+  static constexpr int P_COL = 0;
+  static constexpr int P_GSTRIDE = 32;
   static constexpr bool DQ_ALIAS_DP = D == 128;
-  static constexpr bool P_ALIAS_S = D == 128;
+  static constexpr bool P_ALIAS_S = true;
+  // d = 64: dS'^T also goes to tensor memory (packed bf16, group q at
+  // DST_COL + 16 q), so that dK is a TS MMA and reads only Q from shared
+  // memory.  d = 128 has no columns left: dK reads dS'^T from shared memory.
+  static constexpr bool DK_TS = D == 64;
+  static constexpr int DST_COL = 448;
   // shared memory (offsets from the 1024-B aligned base)
   static constexpr int OFF_K = 0, OFF_V = TILE_BYTES, OFF_Q = 2 * TILE_BYTES;
   static constexpr int OFF_DO = OFF_Q + QST * TILE_BYTES;
@@ -279,11 +283,13 @@ struct BwdCfg {
 //   DSFULL[b]       dS^T_n is in shared-memory buffer b = n % DSST
 //   DSEMPTY[b]      dK and dQ have read buffer b
 //   DQFULL          dQ_n is in tensor memory; DQFREE: the dQ warps have read it
+//   DKDONE          dK += dS'^T_n Q_n is done (the next dS'^T may overwrite TMEM)
 //   QFULL / QEMPTY [n % QST]      ring stage of Q_n (and the -LSE/scale tile)
 //   DOFULL / DOEMPTY [n % DOST]   ring stage of dO_n (and the -D tile)
 enum : int {
   C_KVFULL = 0, C_SFULL, C_SFREE, C_DPFULL, C_DPFREE, C_PFULL, C_PFREE, C_DQFULL, C_DQFREE,
-  C_FINAL, C_DRAIN1, C_DRAIN2, C_DRAIN3, C_DRAIN4, C_DSFULL  // then DSFULL[DSST], DSEMPTY[DSST],
+  C_DKDONE, C_FINAL, C_DRAIN1, C_DRAIN2, C_DRAIN3, C_DRAIN4,
+  C_DSFULL  // then DSFULL[DSST], DSEMPTY[DSST],
                                                               // QFULL[QST], QEMPTY[QST],
                                                               // DOFULL[DOST], DOEMPTY[DOST]
 };
@@ -347,6 +353,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
     mbar_init(bar(C_PFREE), 1);
     mbar_init(bar(C_DQFULL), 1);
     mbar_init(bar(C_DQFREE), 4);  // one arrive per dQ warp
+    mbar_init(bar(C_DKDONE), 1);
     mbar_init(bar(C_FINAL), 2);   // the dV and dK issuers' last commits
     mbar_init(bar(C_DRAIN1), 1);
     mbar_init(bar(C_DRAIN2), 1);
@@ -638,13 +645,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
         if (elect_one()) {
 #pragma unroll
           for (int k = 0; k < C::NK_T; ++k) {
-            const uint32_t off = (k / 4) * C::BLK_BYTES + (k % 4) * 32;
-            mma_ss<MmaKind::kBF16>(tmem + C::DK_COL, sdesc_sw128(sDS(bb) + off, 16, 1024),
-                                   sdesc_sw128(sQ(s) + k * 16 * 128, C::BLK_BYTES, 1024), idDK,
-                                   (n > 0 || k > 0) ? 1u : 0u);
+            const uint64_t bq = sdesc_sw128(sQ(s) + k * 16 * 128, C::BLK_BYTES, 1024);
+            if constexpr (C::DK_TS) {
+              mma_ts<MmaKind::kBF16>(tmem + C::DK_COL, tmem + C::DST_COL + 8 * k, bq, idDK,
+                                     (n > 0 || k > 0) ? 1u : 0u);
+            } else {
+              const uint32_t off = (k / 4) * C::BLK_BYTES + (k % 4) * 32;
+              mma_ss<MmaKind::kBF16>(tmem + C::DK_COL, sdesc_sw128(sDS(bb) + off, 16, 1024), bq,
+                                     idDK, (n > 0 || k > 0) ? 1u : 0u);
+            }
           }
           mma_commit(dsempty(bb));
           mma_commit(qempty(s));
+          mma_commit(bar(C_DKDONE));
         }
         __syncwarp();
         tr.ev(21);
@@ -736,13 +749,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
         if (lane == 0) mbar_arrive(dsfull((n - 1) % DSST));
       }
       tr.ev(38);
-      // the P columns are free once dV_{n-1} has read them
-      if (n > 0 && !mbar_wait_warp(bar(C_PFREE), (n - 1) & 1, abort, 32, status)) {
-        ok = false;
-        break;
-      }
+      // P^T_n goes into this group's S^T columns, already read; S^T_n was
+      // only issued after dV_{n-1} had read P^T_{n-1} there
       tr.ev(39);
-      tc_fence_after();
       tmem_st16(pst, pk);
       tmem_st_wait();
       warp_arrive_tc(bar(C_PFULL));
@@ -777,6 +786,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
         break;
       }
       tr.ev(45);
+      if constexpr (C::DK_TS) {
+        // dS'^T_n to tensor memory for the dK MMA, once dK_{n-1} has read it
+        if (n > 0 && !mbar_wait_warp(bar(C_DKDONE), (n - 1) & 1, abort, 34, status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        tmem_st16(trow + C::DST_COL + 16 * grp, o);
+      }
       // 32 queries = 64 B of this thread's 128-B row of block dsblk, swizzled
       uint8_t* dsrow = smem + C::OFF_DS + (bb * 2 + dsblk) * C::BLK_BYTES + kr * 128;
 #pragma unroll
@@ -784,6 +802,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
         *reinterpret_cast<uint4*>(dsrow + (((dsch0 + c4) ^ (kr & 7)) << 4)) =
             make_uint4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]);
       if (!kDeferDs) {
+        if constexpr (C::DK_TS) {
+          tmem_st_wait();
+          tc_fence_before();
+        }
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) mbar_arrive(dsfull(bb));

@@ -310,9 +310,9 @@ static int prepare_bwd(BwdArgs* a, const void* Q, const void* K, const void* V, 
         (dtype == NEA_BF16 &&
          !encode_3d(&a->tmdQacc, a->dq_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d, N, bh)))
       return NEA_ERR_CUDA;
-    a->status = status_ptr();
-    if (!a->status) return NEA_ERR_CUDA;
   }
+  a->status = status_ptr();  // every stage's kernels report bounded-wait timeouts
+  if (!a->status) return NEA_ERR_CUDA;
   a->Q = Q; a->K = K; a->O = O; a->dO = dO; a->lse = LSE; a->dQ = dQ; a->dK = dK; a->dV = dV;
   a->B = B; a->H = H; a->Hkv = Hkv; a->N = N; a->d = d; a->causal = causal;
   a->scale = scale; a->dtype = dtype;

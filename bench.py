@@ -564,9 +564,10 @@ def _time_ms(fn, l2_flush, stream, reps):
 
 def measure_extras(nea, w, q, k, v, do, o, lse, wsp, l2_flush, stream, peak_hbm, src, reps):
     """The rows beyond the training step: RoPE (rotation pass and the cost of
-    the inverse rotation fused into the backward) on this workload, and
-    decode attention on the decode workloads.  Each is timed alone with CUDA
-    events, L2 flushed before every call."""
+    the inverse rotation fused into the backward) on this workload, the
+    deterministic backward, full attention, the fp32 (TF32) path, and decode
+    attention on the decode workloads.  Each is timed alone with CUDA events,
+    L2 flushed before every call."""
     import torch
     from causal_gqa_flashattention_gb300.workloads import DECODE_WORKLOADS, make_decode_inputs
     out = {}
@@ -594,6 +595,18 @@ def measure_extras(nea, w, q, k, v, do, o, lse, wsp, l2_flush, stream, peak_hbm,
                       "peak_source": f"hbm_gbs of {src}"}
     out["bwd_rope"] = {"ms": round(t_br, 5), "ms_without_rope": round(t_b, 5),
                        "overhead_pct": round(100.0 * (t_br / t_b - 1.0), 2)}
+    # Q rotated inside the forward (K by the pass) against the forward on
+    # pre-rotated inputs; the pass's Q share is its time times Q's byte share
+    of2, lf2 = torch.empty_like(o), torch.empty_like(lse)
+    t_fp = _time_ms(lambda st: nea.attn_fwd(qr, kr, v, out=of2, lse=lf2, stream=st), l2_flush,
+                    stream, reps)
+    t_fq = _time_ms(lambda st: nea.attn_fwd(q, kr, v, out=of2, lse=lf2, stream=st,
+                                            rope_q_cs=cs), l2_flush, stream, reps)
+    out["fwd_rope_q"] = {"ms": round(t_fq, 5), "ms_pre_rotated": round(t_fp, 5),
+                         "overhead_ms": round(t_fq - t_fp, 5),
+                         "pass_q_share_ms": round(t_rot * q.numel() / (q.numel() + k.numel()), 5),
+                         "note": "forward rotating Q in shared memory vs the forward on Qr; "
+                                 "the rotation pass's time for Q alone is its Q byte share"}
     # full (non-causal) attention at the same shape: twice the causal work
     of, lf = torch.empty_like(o), torch.empty_like(lse)
     t_ff = _time_ms(lambda st: nea.attn_fwd(q, k, v, causal=False, out=of, lse=lf, stream=st),
@@ -606,6 +619,33 @@ def measure_extras(nea, w, q, k, v, do, o, lse, wsp, l2_flush, stream, peak_hbm,
                              "tflops": round(full_flops / ((t_ff + t_fb) * 1e-3) / 1e12, 1),
                              "frac_of_peak": round(full_flops / ((t_ff + t_fb) * 1e-3) / 1e12 /
                                                    float(load_peaks()[0]["bf16_tflops"]), 4)}
+    # the fp32 path (TF32 tensor cores) at the GPT-2-small shape: forward and
+    # backward, each timed alone; against the TF32 dense peak, taken as the
+    # measured bf16 peak times the nominal TF32 / bf16 ratio (1.1 / 2.25)
+    from causal_gqa_flashattention_gb300.workloads import WORKLOADS, make_inputs
+    wf = WORKLOADS["gpt2s_f32"]
+    qf, kf, vf, dof = make_inputs(wf, seed=0, device=q.device)
+    of_, lf_ = torch.empty_like(qf), torch.empty((wf.B, wf.H, wf.N), dtype=torch.float32,
+                                                   device=q.device)
+    dqf, dkf, dvf = torch.empty_like(qf), torch.empty_like(kf), torch.empty_like(vf)
+    wsf = torch.empty(nea.bwd_workspace_bytes(wf.B, wf.H, wf.Hkv, wf.N, wf.d, nea.NEA_F32),
+                      dtype=torch.uint8, device=q.device)
+    t_f32f = _time_ms(lambda st: nea.attn_fwd(qf, kf, vf, causal=True, scale=wf.scale, out=of_,
+                                              lse=lf_, stream=st), l2_flush, stream, reps)
+    t_f32b = _time_ms(lambda st: nea.attn_bwd(qf, kf, vf, of_, dof, lf_, causal=True,
+                                              scale=wf.scale, dq=dqf, dk=dkf, dv=dvf,
+                                              workspace=wsf, stream=st), l2_flush, stream, reps)
+    peak_tf32 = float(load_peaks()[0]["bf16_tflops"]) * 1.1 / 2.25
+    tf_f = wf.fwd_flops() / (t_f32f * 1e-3) / 1e12
+    tf_b = wf.bwd_flops() / (t_f32b * 1e-3) / 1e12
+    tf_s = (wf.fwd_flops() + wf.bwd_flops()) / ((t_f32f + t_f32b) * 1e-3) / 1e12
+    out["fp32_tf32_gpt2s"] = {
+        "fwd_ms": round(t_f32f, 5), "bwd_ms": round(t_f32b, 5),
+        "fwd_tflops": round(tf_f, 1), "bwd_tflops": round(tf_b, 1), "tflops": round(tf_s, 1),
+        "roofline": {"bound": "tensor", "peak": round(peak_tf32, 1), "unit": "TFLOP/s",
+                     "frac": round(tf_s / peak_tf32, 4),
+                     "peak_source": f"bf16_tflops of {src} x 1.1 / 2.25 (nominal TF32/bf16)"},
+        "config": workload_config(wf)}
     for name, dw in DECODE_WORKLOADS.items():
         dq_, kc, vc, lens = make_decode_inputs(dw, seed=0, device=q.device)
         od = torch.empty_like(dq_)
@@ -621,7 +661,8 @@ def measure_extras(nea, w, q, k, v, do, o, lse, wsp, l2_flush, stream, peak_hbm,
                      "hbm_frac": round(byt / (t * 1e-3) / 1e9 / peak_hbm, 3),
                      "config": {"B": dw.B, "H": dw.H, "Hkv": dw.Hkv, "nq": dw.nq,
                                 "Lmax": dw.Lmax, "d": dw.d, "dtype": dw.dtype},
-                     "peak_source": f"hbm_gbs of {src}", "launches": 2}
+                     "peak_source": f"hbm_gbs of {src}",
+                     "launches": 1 if -(-dw.Lmax // 128) <= 16 else 2}
     return out
 
 

@@ -16,6 +16,8 @@
 //                  P V (thread = output column) into the workspace;
 //  decode_combine  per query row, rescales the chunks' partials to the
 //                  common max and normalises: O (dtype) and LSE (natural log).
+// A short cache runs the first kernel alone: the splits of a (batch, KV
+// head) form a thread-block cluster and fold their results on chip.
 #include <algorithm>
 
 #include <cuda_bf16.h>
@@ -94,7 +96,15 @@ __device__ __forceinline__ int cache_len(const DecodeArgs& a, int b) {
 // scores (thread = cache row), the chunk's row max and P, then P V (warp w
 // owns rows w, w + 4, ...; lane l owns CPL adjacent columns) folded into a
 // running (max, sum, O) per row -- the online softmax across the split.
-template <typename T, int D, int RM, int STAGES>
+//
+// CLUSTER (a short cache): the splits of one (batch, KV head) form a thread-
+// block cluster (gridDim.x = the splits = the cluster's size).  Each leaves
+// its running (max, sum, O) per row in its own shared memory; after a
+// cluster barrier, rank 0 folds them together through distributed shared
+// memory and writes O and LSE: one launch, no partials in global memory, no
+// combine kernel.  A split past its element's cache, and a CTA unwinding
+// after a timeout, still meet the cluster at both barriers.
+template <typename T, int D, int RM, int STAGES, bool CLUSTER>
 __global__ void __launch_bounds__(kChunk) decode_partial_kernel(const __grid_constant__ DecodeArgs a) {
   constexpr int ES = static_cast<int>(sizeof(T));
   constexpr int TILE = kChunk * D * ES;     // one K or V tile
@@ -117,8 +127,8 @@ __global__ void __launch_bounds__(kChunk) decode_partial_kernel(const __grid_con
   const int nvc = (L + kChunk - 1) / kChunk;  // chunks holding valid rows
   const int cb = split * a.cps;
   const int ce = min(cb + a.cps, nvc);
-  if (cb >= ce) return;  // past this element's cache: the combine skips the split
-  const int n = ce - cb;
+  if (!CLUSTER && cb >= ce) return;  // past this element's cache: the combine skips the split
+  const int n = ce > cb ? ce - cb : 0;
   volatile int* abort = &abort_sh;
   auto sK = [&](int s) { return smem + 2 * s * TILE; };
   auto sV = [&](int s) { return smem + (2 * s + 1) * TILE; };
@@ -334,8 +344,54 @@ __global__ void __launch_bounds__(kChunk) decode_partial_kernel(const __grid_con
     if (tid == 0)
       for (int it = issued > STAGES ? issued - STAGES : 0; it < issued; ++it)
         mbar_wait_drain(smem_u32(&full[it % STAGES]), (it / STAGES) & 1, 91, a.status);
-    return;
+    if (!CLUSTER) return;
   }
+  if constexpr (CLUSTER) {
+    // this split's (max, sum, O) per row into the first stage (every load
+    // has landed and been read), [RM][D] then [RM][2]
+    __syncthreads();
+    float* cl_o = reinterpret_cast<float*>(smem);
+    float* cl_ml = cl_o + RM * D;
+#pragma unroll
+    for (int i = 0; i < RW; ++i) {
+      const int r = warp + 4 * i;
+      if (r < R) {
+#pragma unroll
+        for (int cc = 0; cc < CPL / 2; ++cc) {
+          cl_o[r * D + CPL * lane + 2 * cc] = o[i][cc].x;
+          cl_o[r * D + CPL * lane + 2 * cc + 1] = o[i][cc].y;
+        }
+        if (lane == 0) {
+          cl_ml[2 * r] = m_run[i];
+          cl_ml[2 * r + 1] = l_run[i];
+        }
+      }
+    }
+    cluster_sync();
+    if (split == 0 && ok) {
+      // rank 0: fold the splits row by row (thread = column, rows in turn)
+      const uint32_t o_base = smem_u32(cl_o), ml_base = smem_u32(cl_ml);
+      const int nsp = gridDim.x;
+      for (int e = tid; e < R * D; e += kChunk) {
+        const int r = e / D, col = e % D;
+        float M = -INFINITY;
+        for (int q = 0; q < nsp; ++q)
+          M = fmaxf(M, ld_shared_cluster_f32(mapa_shared(ml_base + 8 * r, q)));
+        float lt = 0.f, ot = 0.f;
+        for (int q = 0; q < nsp; ++q) {
+          const float m = ld_shared_cluster_f32(mapa_shared(ml_base + 8 * r, q));
+          const float w = m == -INFINITY ? 0.f : exp2f(m - M);
+          lt = fmaf(w, ld_shared_cluster_f32(mapa_shared(ml_base + 8 * r + 4, q)), lt);
+          ot = fmaf(w, ld_shared_cluster_f32(mapa_shared(o_base + 4 * (r * D + col), q)), ot);
+        }
+        const int gi = r / a.nq, t = r % a.nq;
+        const size_t row = (static_cast<size_t>(b) * a.H + g * G + gi) * a.nq + t;
+        from_f(ot / lt, static_cast<T*>(a.O) + row * D + col);
+        if (col == 0) a.lse[row] = (M + log2f(lt)) * kLn2;
+      }
+    }
+    cluster_sync();  // the other splits' shared memory stays until rank 0 has read it
+  } else {
 #pragma unroll
   for (int i = 0; i < RW; ++i) {
     const int r = warp + 4 * i;
@@ -350,6 +406,7 @@ __global__ void __launch_bounds__(kChunk) decode_partial_kernel(const __grid_con
       }
       if (lane == 0) a.ml[row * a.nchunk + split] = make_float2(m_run[i], l_run[i]);
     }
+  }
   }
 }
 
@@ -417,7 +474,7 @@ cudaError_t launch_partial(DecodeArgs& a, int sms, cudaStream_t stream) {
   constexpr int STAGES = 1;
   const int smem = 1024 + 2 * STAGES * TILE + (RM * D + RM * kChunk + 8 * RM) * 4 +
                    (RM == 4 ? 16 * D * 4 : 0);
-  auto kp = decode_partial_kernel<T, D, RM, STAGES>;
+  auto kp = decode_partial_kernel<T, D, RM, STAGES, false>;
   cudaError_t e = cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   int per_sm = 1;
@@ -433,9 +490,46 @@ cudaError_t launch_partial(DecodeArgs& a, int sms, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// A short cache (at most kClusterChunks chunks): up to 8 splits of one
+// (batch, KV head) run as a cluster and fold their results on chip.
+constexpr int kClusterChunks = 16;
+template <typename T, int D, int RM>
+cudaError_t launch_cluster(DecodeArgs& a, cudaStream_t stream) {
+  constexpr int TILE = kChunk * D * static_cast<int>(sizeof(T));
+  constexpr int STAGES = 4 * TILE <= 128 * 1024 ? 2 : 1;  // (fp32 at d = 128: one)
+  static_assert((RM * D + 2 * RM) * 4 <= TILE, "the split's results fit in the first stage");
+  const int smem = 1024 + 2 * STAGES * TILE + (RM * D + RM * kChunk + 8 * RM) * 4 +
+                   (RM == 4 ? 16 * D * 4 : 0);
+  auto kp = decode_partial_kernel<T, D, RM, STAGES, true>;
+  cudaError_t e = cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int chunks = a.nchunk;
+  const int nsplit = std::min(chunks, 8);
+  a.cps = (chunks + nsplit - 1) / nsplit;
+  a.nchunk = (chunks + a.cps - 1) / a.cps;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.nchunk, a.B * a.Hkv);
+  cfg.blockDim = dim3(kChunk);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = a.nchunk;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kp, a);
+}
+
 template <typename T, int D>
 cudaError_t launch_t(DecodeArgs a, int sms, cudaStream_t stream) {
   const int R = (a.H / a.Hkv) * a.nq;
+  if (a.nchunk <= kClusterChunks)
+    return R <= 4    ? launch_cluster<T, D, 4>(a, stream)
+           : R <= 8  ? launch_cluster<T, D, 8>(a, stream)
+           : R <= 16 ? launch_cluster<T, D, 16>(a, stream)
+                     : launch_cluster<T, D, kMaxDecodeRows>(a, stream);
   cudaError_t e = R <= 4    ? launch_partial<T, D, 4>(a, sms, stream)
                   : R <= 8  ? launch_partial<T, D, 8>(a, sms, stream)
                   : R <= 16 ? launch_partial<T, D, 16>(a, sms, stream)

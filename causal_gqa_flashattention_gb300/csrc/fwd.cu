@@ -280,7 +280,9 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
       Tracer tr(NEA_TRACE_FWD, traced, 1);
       constexpr uint32_t idS = make_idesc<KIND>(128, 128, false, false);
       constexpr uint32_t idPV = make_idesc<KIND>(128, D, false, !C::TRANSPOSE_V);
-      const int qbar = C::TRANSPOSE_V ? B_QREADY : B_QFULL;
+      // Q is usable once it has landed, or once it has been rounded (tf32)
+      // or rotated (RoPE) in shared memory
+      const int qbar = (C::TRANSPOSE_V || a.rope_cs != nullptr) ? B_QREADY : B_QFULL;
       // S for global tile g = tile j of item `it`.  After an item's last S,
       // QEMPTY hands Q's buffer back to the producer.
       auto issue_s = [&](int g, const FwdItem& it, int j) -> bool {
@@ -473,6 +475,37 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
     FwdItem it;
     for (int k = 0; k < kMaxItems && fwd_item(a, T, k, it); ++k) {
       float m_ref = -INFINITY, l = 0.f;
+      if (KIND == MmaKind::kBF16 && a.rope_cs != nullptr) {
+        // RoPE: rotate row r of this item's Q tile in place (pairs within a
+        // 16-byte chunk of the 128-byte swizzled row; fp32 arithmetic, one
+        // rounding), then hand the tile to the MMA warp (QREADY).  The next
+        // item's first S then waits for this rotation.
+        ok = ok && mbar_wait_warp(bar(B_QFULL), k & 1, abort, 13, status);
+        const int n = it.qt * kTile + r;  // position of this query row
+        if (ok && n < a.N) {
+          const float4* cs4 = reinterpret_cast<const float4*>(a.rope_cs + static_cast<size_t>(n) * (D / 2));
+#pragma unroll
+          for (int ch = 0; ch < D / 8; ++ch) {
+            uint8_t* p = smem + (ch / 8) * C::BLK_BYTES + r * 128 + (((ch % 8) ^ (r & 7)) << 4);
+            uint4 w = *reinterpret_cast<const uint4*>(p);
+            uint32_t* wv = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const float4 t = __ldg(cs4 + 2 * ch + h2);  // pairs 4 ch + 2 h2, + 1
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const float ct = e == 0 ? t.x : t.z, st = e == 0 ? t.y : t.w;
+                const uint32_t x = wv[2 * h2 + e];
+                const float a0 = __uint_as_float(x << 16), b0 = __uint_as_float(x & 0xffff0000u);
+                wv[2 * h2 + e] = pack_bf16(fmaf(a0, ct, -(b0 * st)), fmaf(a0, st, b0 * ct));
+              }
+            }
+            *reinterpret_cast<uint4*>(p) = w;
+          }
+        }
+        fence_proxy_async();
+        mbar_arrive(bar(B_QREADY));
+      }
       for (int j = 0; ok && j < it.nkv; ++j, ++g) {
         if (!mbar_wait_warp(bar(B_SFULL), g & 1, abort, 9, status)) {
           ok = false;

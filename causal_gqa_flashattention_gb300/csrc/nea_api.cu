@@ -241,8 +241,9 @@ const char* nea_status_string(int status) {
   }
 }
 
-int nea_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
-                 int Hkv, int N, int d, float scale, int causal, int dtype, void* stream) {
+static int attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                    const float* rope_cs, int B, int H, int Hkv, int N, int d, float scale,
+                    int causal, int dtype, void* stream) {
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE))
     return NEA_ERR_INVALID;
   int st = check_common(B, H, Hkv, N, d, scale, causal, dtype, /*bwd=*/false);
@@ -257,6 +258,7 @@ int nea_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LS
       !encode_3d(&a.tmV, V, dt, es, d, N, bkv) || !encode_3d(&a.tmO, O, dt, es, d, N, bh))
     return NEA_ERR_CUDA;
   a.lse = LSE;
+  a.rope_cs = reinterpret_cast<const float2*>(rope_cs);
   a.status = status_ptr();
   if (!a.status) return NEA_ERR_CUDA;
   a.B = B; a.H = H; a.Hkv = Hkv; a.N = N; a.d = d; a.causal = causal;
@@ -264,6 +266,19 @@ int nea_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LS
   return launch_fwd(a, sm_count(), static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? NEA_OK
              : NEA_ERR_CUDA;
+}
+
+int nea_attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                 int Hkv, int N, int d, float scale, int causal, int dtype, void* stream) {
+  return attn_fwd(Q, K, V, O, LSE, nullptr, B, H, Hkv, N, d, scale, causal, dtype, stream);
+}
+
+int nea_attn_fwd_rope_q(const void* Q, const void* Kr, const void* V, void* O, float* LSE,
+                        const float* cos_sin, int B, int H, int Hkv, int N, int d, float scale,
+                        int causal, int dtype, void* stream) {
+  if (!aligned16(cos_sin)) return NEA_ERR_INVALID;
+  if (dtype != NEA_BF16) return NEA_ERR_UNSUPPORTED;
+  return attn_fwd(Q, Kr, V, O, LSE, cos_sin, B, H, Hkv, N, d, scale, causal, dtype, stream);
 }
 
 size_t nea_attn_bwd_workspace_bytes(int B, int H, int Hkv, int N, int d, int dtype) {

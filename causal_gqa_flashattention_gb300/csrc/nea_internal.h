@@ -18,6 +18,8 @@ struct FwdArgs {
   int B, H, Hkv, N, d, causal;
   float scale;                     // softmax scale
   int dtype;                       // 0 bf16, 1 fp32
+  const float2* rope_cs;           // null, or RoPE (cos, sin) [N][d/2]: Q is rotated in
+                                   // shared memory before its first S (bf16 only)
 };
 
 struct BwdArgs {

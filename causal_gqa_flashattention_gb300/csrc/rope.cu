@@ -7,10 +7,14 @@
 //
 //  rope_table   cs[n][i] = (cos, sin)(n * theta_i), angles in fp64, stored
 //               as fp32 pairs [N][d/2];
-//  rope_rotate  Qr = R(Q), Kr = R(K) in one launch, one 16-byte chunk of a
-//               row per thread (fp32 arithmetic, one rounding to the dtype).
+//  rope_rotate  Qr = R(Q), Kr = R(K) in one launch: a thread rotates one
+//               16-byte column chunk of one position in several heads with
+//               one load of its (cos, sin) pairs (fp32 arithmetic, one
+//               rounding to the dtype).
 // The attention kernels then run on Qr and Kr unchanged; the backward maps
 // dQr, dKr back with the transposed rotation in its own epilogues.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 
 #include "nea_internal.h"
@@ -65,38 +69,63 @@ struct Chunk<float> {
   }
 };
 
-// Chunks [0, n0) belong to (x0 -> y0), chunks [n0, n0 + n1) to (x1 -> y1).
+// Thread = (position n, 16-byte column chunk) x a group of kRopeHeads
+// heads: it loads the chunk's (cos, sin) pairs once and reuses them for the
+// same chunk of row n of each of its heads, with all of those rows' loads
+// in flight before the first store.  Heads [0, h0) are rows of x0 -> y0
+// (Q), heads [h0, h0 + h1) rows of x1 -> y1 (K); each head has N rows.
+#ifndef NEA_ROPE_HEADS
+#define NEA_ROPE_HEADS 4
+#endif
+constexpr int kRopeHeads = NEA_ROPE_HEADS;
+
 template <typename T>
 __global__ void __launch_bounds__(256) rope_rotate_kernel(const T* __restrict__ x0, T* y0,
-                                                          long long n0, const T* __restrict__ x1,
-                                                          T* y1, long long n1,
+                                                          long long h0, const T* __restrict__ x1,
+                                                          T* y1, long long h1,
                                                           const float2* __restrict__ cs, int N,
                                                           int d) {
   constexpr int E = Chunk<T>::E;
-  long long c = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
-  const T* x = x0;
-  T* y = y0;
-  if (c >= n0) {
-    c -= n0;
-    if (c >= n1) return;
-    x = x1;
-    y = y1;
-  }
   const int cpr = d / E;  // chunks per row
-  const long long row = c / cpr;
-  const int col = static_cast<int>(c - row * cpr) * E;
-  const int n = static_cast<int>(row % N);
-  const float2* t = cs + static_cast<size_t>(n) * (d / 2) + col / 2;
-  float v[E];
-  Chunk<T>::load(x + c * E, v);
+  const long long c = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
+  if (c >= static_cast<long long>(N) * cpr) return;
+  const int n = static_cast<int>(c / cpr);
+  const int col = static_cast<int>(c - static_cast<long long>(n) * cpr) * E;
+  float2 r[E / 2];
+  const float4* t = reinterpret_cast<const float4*>(cs + static_cast<size_t>(n) * (d / 2) + col / 2);
 #pragma unroll
-  for (int k = 0; k < E / 2; ++k) {
-    const float2 r = __ldg(t + k);
-    const float a = v[2 * k], b = v[2 * k + 1];
-    v[2 * k] = fmaf(a, r.x, -(b * r.y));
-    v[2 * k + 1] = fmaf(a, r.y, b * r.x);
+  for (int k = 0; k < E / 4; ++k) {  // two pairs per 16-byte load
+    const float4 w = __ldg(t + k);
+    r[2 * k] = make_float2(w.x, w.y);
+    r[2 * k + 1] = make_float2(w.z, w.w);
   }
-  Chunk<T>::store(y + c * E, v);
+  for (long long hb = static_cast<long long>(blockIdx.y) * kRopeHeads; hb < h0 + h1;
+       hb += static_cast<long long>(gridDim.y) * kRopeHeads) {
+  float v[kRopeHeads][E];
+#pragma unroll
+  for (int u = 0; u < kRopeHeads; ++u) {
+    const long long h = hb + u;
+    if (h < h0 + h1) {
+      const T* x = h < h0 ? x0 + (h * N + n) * static_cast<long long>(d)
+                          : x1 + ((h - h0) * N + n) * static_cast<long long>(d);
+      Chunk<T>::load(x + col, v[u]);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kRopeHeads; ++u) {
+    const long long h = hb + u;
+    if (h >= h0 + h1) continue;
+#pragma unroll
+    for (int k = 0; k < E / 2; ++k) {
+      const float a = v[u][2 * k], b = v[u][2 * k + 1];
+      v[u][2 * k] = fmaf(a, r[k].x, -(b * r[k].y));
+      v[u][2 * k + 1] = fmaf(a, r[k].y, b * r[k].x);
+    }
+    T* y = h < h0 ? y0 + (h * N + n) * static_cast<long long>(d)
+                  : y1 + ((h - h0) * N + n) * static_cast<long long>(d);
+    Chunk<T>::store(y + col, v[u]);
+  }
+  }
 }
 
 }  // namespace
@@ -112,16 +141,18 @@ cudaError_t launch_rope_rotate(const void* Q, const void* K, void* Qr, void* Kr,
                                const float2* cs, long long qrows, long long krows, int N, int d,
                                int dtype, cudaStream_t stream) {
   const int E = dtype == 0 ? 8 : 4;
-  const long long n0 = qrows * (d / E), n1 = krows * (d / E);
-  const unsigned grid = static_cast<unsigned>((n0 + n1 + 255) / 256);
+  const long long h0 = qrows / N, h1 = krows / N;  // heads of Q, of K
+  const dim3 grid(static_cast<unsigned>((static_cast<long long>(N) * (d / E) + 255) / 256),
+                  static_cast<unsigned>(std::min<long long>((h0 + h1 + kRopeHeads - 1) / kRopeHeads,
+                                                            65535)));
   if (dtype == 0)
     rope_rotate_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(Q), static_cast<__nv_bfloat16*>(Qr), n0,
-        static_cast<const __nv_bfloat16*>(K), static_cast<__nv_bfloat16*>(Kr), n1, cs, N, d);
+        static_cast<const __nv_bfloat16*>(Q), static_cast<__nv_bfloat16*>(Qr), h0,
+        static_cast<const __nv_bfloat16*>(K), static_cast<__nv_bfloat16*>(Kr), h1, cs, N, d);
   else
     rope_rotate_kernel<float><<<grid, 256, 0, stream>>>(
-        static_cast<const float*>(Q), static_cast<float*>(Qr), n0, static_cast<const float*>(K),
-        static_cast<float*>(Kr), n1, cs, N, d);
+        static_cast<const float*>(Q), static_cast<float*>(Qr), h0, static_cast<const float*>(K),
+        static_cast<float*>(Kr), h1, cs, N, d);
   return cudaGetLastError();
 }
 

@@ -71,6 +71,8 @@ def load_library(path):
     L.nea_attn_bwd_finalize.restype = _i
     L.nea_rope_table.argtypes = [_vp, _i, _i, ctypes.c_double, _vp]
     L.nea_rope_table.restype = _i
+    L.nea_attn_fwd_rope_q.argtypes = [_vp] * 6 + [_i] * 5 + [ctypes.c_float] + [_i] * 2 + [_vp]
+    L.nea_attn_fwd_rope_q.restype = _i
     L.nea_rope_qk.argtypes = [_vp] * 5 + [_i] * 6 + [_vp]
     L.nea_rope_qk.restype = _i
     L.nea_attn_bwd_rope.argtypes = [_vp] * 11 + [ctypes.c_size_t] + [_i] * 5 + [
@@ -134,17 +136,28 @@ def _check(q, k, v):
     return B, H, Hkv, N, d
 
 
-def attn_fwd(q, k, v, *, causal=True, scale=None, out=None, lse=None, stream=None):
-    """O, LSE = attention(q, k, v).  q [B,H,N,d], k/v [B,Hkv,N,d] (bf16)."""
+def attn_fwd(q, k, v, *, causal=True, scale=None, out=None, lse=None, stream=None,
+             rope_q_cs=None):
+    """O, LSE = attention(q, k, v).  q [B,H,N,d], k/v [B,Hkv,N,d] (bf16).
+
+    With ``rope_q_cs`` (a RoPE table), ``q`` is the unrotated Q, ``k`` the
+    rotated K, and the kernel rotates Q itself (nea_attn_fwd_rope_q)."""
     B, H, Hkv, N, d = _check(q, k, v)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     o = torch.empty_like(q) if out is None else out
     lse_t = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
-    st = lib().nea_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse_t), B, H, Hkv, N, d,
-                            scale, int(bool(causal)), _dtype_code(q),
-                            ctypes.c_void_p(_stream_handle(stream)))
+    s = ctypes.c_void_p(_stream_handle(stream))
+    if rope_q_cs is None:
+        st = lib().nea_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse_t), B, H, Hkv, N, d,
+                                scale, int(bool(causal)), _dtype_code(q), s)
+        what = "nea_attn_fwd"
+    else:
+        st = lib().nea_attn_fwd_rope_q(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse_t),
+                                       _ptr(rope_q_cs), B, H, Hkv, N, d, scale,
+                                       int(bool(causal)), _dtype_code(q), s)
+        what = "nea_attn_fwd_rope_q"
     if st != NEA_OK:
-        raise NeaError(st, "nea_attn_fwd")
+        raise NeaError(st, what)
     return o, lse_t
 
 

@@ -207,6 +207,21 @@ int nea_rope_qk(const void* Q, const void* K, void* Qr, void* Kr, const float* c
                 int H, int Hkv, int N, int d, int dtype, void* stream);
 
 /*
+ * Forward with the rotation of Q done inside the kernel: Q is the caller's
+ * unrotated Q, Kr the rotated K (e.g. from nea_rope_qk()), cos_sin the
+ * table; O and LSE are those of nea_attn_fwd() on (R(Q), Kr, V).  Each
+ * query tile is rotated in shared memory once it has landed, before its
+ * first S = Q K^T (fp32 arithmetic, one rounding to bf16, as
+ * nea_rope_qk()), so R(Q) is never written to memory.  bf16 only (fp32:
+ * NEA_ERR_UNSUPPORTED); cos_sin 16-byte aligned, else NEA_ERR_INVALID;
+ * other arguments as nea_attn_fwd().  The backward needs R(Q) itself
+ * (nea_attn_bwd_rope() takes Qr, Kr).
+ */
+int nea_attn_fwd_rope_q(const void* Q, const void* Kr, const void* V, void* O, float* LSE,
+                        const float* cos_sin, int B, int H, int Hkv, int N, int d, float scale,
+                        int causal, int dtype, void* stream);
+
+/*
  * Backward of attention on rotated inputs.  Arguments as nea_attn_bwd(),
  * with Qr, Kr the rotated Q and K the forward ran on, and cos_sin the table
  * they were rotated with.  dV is as nea_attn_bwd() gives it; dQ and dK are

@@ -5,7 +5,8 @@ bf16 once): O max-abs <= 2e-2, LSE max-abs <= 1e-3.  fp32 (all fp32 CUDA-core
 arithmetic, sums of at most Lmax terms): O relative L2 <= 1e-5, LSE max-abs
 <= 1e-5.  Cases: ragged cache lengths from 1 row to the whole cache, several
 new tokens per sequence, grouped and plain heads, d = 64 and 128, and the
-GPT-2-small decode step.
+GPT-2-small decode step; caches of at most 16 chunks of 128 rows (one
+launch, one CTA per (batch, KV head)) and longer ones (split, then combine).
 """
 import numpy as np
 import pytest
@@ -32,6 +33,9 @@ CASES = [
     DecodeWorkload("mha_f32", 3, 6, 6, 2, 4096, 64, "f32", (4096, 129, 2)),
     DecodeWorkload("gqa8_f32_d128", 2, 16, 2, 2, 640, 128, "f32", (640, 257)),
     DECODE_WORKLOADS["decode_gpt2s_bf16"],
+    # past 16 chunks of 128 rows: split over the cache, then the combine
+    DecodeWorkload("split_bf16_nq2", 2, 12, 4, 2, 6144, 64, "bf16", (6144, 2050)),
+    DecodeWorkload("split_bf16_d128", 1, 8, 2, 1, 2177, 128, "bf16", (2177,)),
 ]
 
 

@@ -92,3 +92,32 @@ def test_backward_through_rotation(nea, w):
     assert max(errs.values()) <= tol, errs
     # the unrotated gradients differ from the rotated ones (the mapping ran)
     assert rel_l2(dq, dqr) > 0.05 and rel_l2(dk, dkr) > 0.05
+
+
+@pytest.mark.parametrize("w", [custom(2, 6, 2, 384, 64), custom(1, 4, 2, 300, 128, causal=False),
+                               custom(1, 3, 1, 77, 64), custom(4, 12, 4, 1000, 64)],
+                         ids=lambda w: w.name)
+def test_forward_rotating_q_in_kernel(nea, w):
+    """nea_attn_fwd_rope_q (Q rotated in shared memory, K by the pass): bit-
+    identical to the forward on the pass's rotated Q (the same fp32
+    arithmetic and one rounding to bf16 feed the same MMAs), and, like every
+    forward, within the forward tolerances (O max-abs 2e-2, LSE max-abs 1e-3)
+    of the oracle on the same bf16 inputs: the pass's Qr and Kr, which
+    test_rotation_matches_oracle pins to oracle.rope within one bf16 ulp."""
+    dev = torch.device("cuda:0")
+    q, k, v, _ = make_inputs(w, seed=5, device=dev)
+    cs = nea.rope_table(w.N, w.d, device=dev)
+    qr, kr = nea.rope_qk(q, k, cs)
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((w.B, w.H, w.N), float("nan"), device=dev)
+    nea.attn_fwd(q, kr, v, causal=w.causal, scale=w.scale, out=o, lse=lse, rope_q_cs=cs)
+    o2, lse2 = nea.attn_fwd(qr, kr, v, causal=w.causal, scale=w.scale)
+    torch.cuda.synchronize()
+    assert nea.check_status() == 0
+    ro, rlse = oracle.attn_fwd(qr.cpu(), kr.cpu(), v.cpu(), w.scale, w.causal)
+    og = o.float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(og).all()
+    assert np.abs(og - ro).max() <= 2e-2
+    assert np.abs(lse.cpu().numpy().astype(np.float64) - rlse).max() <= 1e-3
+    # the in-kernel rotation rounds exactly like the pass: same inputs to the MMAs
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)

@@ -470,10 +470,12 @@ def run_cuda(args):
     main_flops = w.bwd_flops()
     main_tf = main_flops / (k_ms[2] * 1e-3) / 1e12
     rows = w.B * w.H * w.N
-    # bf16: the preprocess also clears the fp32 dQ accumulator and the cast
-    # reads it back; fp32: the dQ kernel writes dQ directly (no cast)
+    # bf16: the preprocess also writes the row-term tiles (32 bytes per row)
+    # and clears the fp32 dQ accumulator, which the cast reads back; fp32:
+    # the dQ kernel writes dQ directly (no cast)
     acc = rows * w.d * 4 if w.dtype == "bf16" else 0
-    pre_bytes = 2 * rows * w.d * w.esize + rows * 4 + 2 * rows * 4 + acc
+    fold = 32 * rows if w.dtype == "bf16" else 0
+    pre_bytes = 2 * rows * w.d * w.esize + rows * 4 + 2 * rows * 4 + fold + acc
     post_bytes = max(acc + rows * w.d * w.esize if acc else 0, 1)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws,

@@ -46,6 +46,19 @@ constexpr float kLog2e = 1.4426950408889634f;
 // mask): rows 0 producer, 1 / 2 MMA issuers, 3 / 4 first warp of each compute
 // warpgroup, 5 first dQ warp.
 __device__ long long g_trace_bwd[kTraceRoles * kTraceEvents];
+// Every CTA of the main kernel: (start, end) in global nanoseconds and its SM.
+constexpr int kTraceCtas = 4096;
+__device__ long long g_trace_cta[3 * kTraceCtas];
+__device__ __forceinline__ long long global_ns() {
+  long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ int sm_id() {
+  int v;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(v));
+  return v;
+}
 #define NEA_TRACE_BASE g_trace_bwd
 #else
 #define NEA_TRACE_BASE nullptr
@@ -372,13 +385,37 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
       mbar_init(doempty(s), 2);  // read by dP (issuer 1) and dV (issuer 2)
     }
     fence_barrier_init();
-  }
-  if (warp == 0 && lane == 0) {
+    // The CTA's first loads go out now, before the TMEM allocation and the
+    // shared-memory setup below: K_j and V_j, and the first ring stages of
+    // Q and dO with their row-term tiles (the producer loop continues from
+    // there).  Their latency is most of a short CTA's fixed cost.
     prefetch_tmap(&a.tmQ);
     prefetch_tmap(&a.tmK);
     prefetch_tmap(&a.tmV);
     prefetch_tmap(&a.tmdO);
     prefetch_tmap(&a.tmdQacc);
+    const int kvh = b * a.Hkv + g;
+    mbar_expect_tx(bar(C_KVFULL), 2 * C::TILE_BYTES);
+    for (int k = 0; k < C::NBLK; ++k) {
+      tma_load_3d(sK + k * C::BLK_BYTES, &a.tmK, bar(C_KVFULL), k * 64, j * kTile, kvh);
+      tma_load_3d(sV + k * C::BLK_BYTES, &a.tmV, bar(C_KVFULL), k * 64, j * kTile, kvh);
+    }
+    for (int n = 0; n < QST && n < nsteps; ++n) {
+      const int h = g * G + n / nI, i = i0 + n % nI, bh = b * a.H + h;
+      const uint16_t* fold = a.fold + (static_cast<size_t>(bh) * T + i) * 2048;
+      mbar_expect_tx(qfull(n), C::TILE_BYTES + 2048);
+      for (int k = 0; k < C::NBLK; ++k)
+        tma_load_3d(sQ(n) + k * C::BLK_BYTES, &a.tmQ, qfull(n), k * 64, i * kTile, bh);
+      bulk_load(sFU(n), fold, 2048, qfull(n));
+    }
+    for (int n = 0; n < DOST && n < nsteps; ++n) {
+      const int h = g * G + n / nI, i = i0 + n % nI, bh = b * a.H + h;
+      const uint16_t* fold = a.fold + (static_cast<size_t>(bh) * T + i) * 2048;
+      mbar_expect_tx(dofull(n), C::TILE_BYTES + 2048);
+      for (int k = 0; k < C::NBLK; ++k)
+        tma_load_3d(sDO(n) + k * C::BLK_BYTES, &a.tmdO, dofull(n), k * 64, i * kTile, bh);
+      bulk_load(sFW(n), fold + 1024, 2048, dofull(n));
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&tmem_base_sh), 512);
@@ -407,6 +444,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
   auto p_col = [&](int k) { return C::P_COL + (k / 2) * C::P_GSTRIDE + (k % 2) * 8; };
 
   const bool traced = blockIdx.x == 0 && lane == 0;
+#ifdef NEA_TRACE
+  if (threadIdx.x == 0 && blockIdx.x < kTraceCtas) {
+    g_trace_cta[3 * blockIdx.x] = global_ns();
+    g_trace_cta[3 * blockIdx.x + 2] = sm_id();
+  }
+#endif
   if (warp == 0) {
     // ------------------------------------------------------------ producer + dQ issuer
     // One warp runs two roles without blocking on either: it issues
@@ -420,17 +463,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
       Tracer tr(NEA_TRACE_BASE, traced, 0);
       Tracer trq(NEA_TRACE_BASE, traced, 7);
       tr.ev(0);
-      const int kvh = b * a.Hkv + g;
-      if (elect_one()) {
-        mbar_expect_tx(bar(C_KVFULL), 2 * C::TILE_BYTES);
-        for (int k = 0; k < C::NBLK; ++k) {
-          tma_load_3d(sK + k * C::BLK_BYTES, &a.tmK, bar(C_KVFULL), k * 64, j * kTile, kvh);
-          tma_load_3d(sV + k * C::BLK_BYTES, &a.tmV, bar(C_KVFULL), k * 64, j * kTile, kvh);
-        }
-      }
-      __syncwarp();
       constexpr uint32_t idDQ = make_idesc<MmaKind::kBF16>(128, D, true, true);
-      int nl = 0, nd = 0, nq = DQ ? 0 : nsteps;  // next step to load Q / dO / issue dQ for
+      // next step to load Q / dO for (the prologue issued the first stages),
+      // and to issue dQ for
+      int nl = QST < nsteps ? QST : nsteps, nd = DOST < nsteps ? DOST : nsteps;
+      int nq = DQ ? 0 : nsteps;
       bool ok = true;
       long long idle0 = clock64();
       while (nl < nsteps || nd < nsteps || nq < nsteps) {
@@ -922,8 +959,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
       }
       tr.ev(42);
     }
+    // the staging buffer must stay until the last reductions have read it;
+    // their writes complete with the grid
     if (lead_warp) {
-      if (elect_one()) bulk_wait0();
+      if (elect_one()) bulk_wait_read0();
       __syncwarp();
     }
   }
@@ -934,6 +973,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+#ifdef NEA_TRACE
+  if (threadIdx.x == 0 && blockIdx.x < kTraceCtas) g_trace_cta[3 * blockIdx.x + 1] = global_ns();
+#endif
 }
 
 
@@ -1006,5 +1048,11 @@ extern "C" int nea_trace_read_bwd(long long* host) {
     return -1;
   static long long zeros[nea::kTraceRoles * nea::kTraceEvents] = {};
   return cudaMemcpyToSymbol(nea::g_trace_bwd, zeros, sizeof(zeros)) == cudaSuccess ? 0 : -1;
+}
+// Copies (start ns, end ns, SM) of the main kernel's first kTraceCtas CTAs.
+extern "C" int nea_trace_read_cta(long long* host) {
+  return cudaMemcpyFromSymbol(host, nea::g_trace_cta, sizeof(nea::g_trace_cta)) == cudaSuccess
+             ? 0
+             : -1;
 }
 #endif

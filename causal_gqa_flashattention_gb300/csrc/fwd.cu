@@ -696,8 +696,10 @@ __global__ void __launch_bounds__(FwdCfg<D, KIND>::THREADS, FwdCfg<D, KIND>::CTA
         __syncwarp();
       }
     }  // items
+    // the staging buffer must stay until the last store has read it; its
+    // writes complete with the grid
     if (warp == 2) {
-      if (elect_one()) bulk_wait0();
+      if (elect_one()) bulk_wait_read0();
       __syncwarp();
     }
   }

@@ -535,6 +535,8 @@ def _time_ms(fn, l2_flush, stream, reps):
     launch work does not land inside the events (eager launches if capture
     fails)."""
     import torch
+    fn(stream)  # one eager call first (a library's lazily created resources exist before capture)
+    torch.cuda.synchronize()
     g = None
     try:
         g = torch.cuda.CUDAGraph()

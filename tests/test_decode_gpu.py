@@ -36,6 +36,9 @@ CASES = [
     # past 16 chunks of 128 rows: split over the cache, then the combine
     DecodeWorkload("split_bf16_nq2", 2, 12, 4, 2, 6144, 64, "bf16", (6144, 2050)),
     DecodeWorkload("split_bf16_d128", 1, 8, 2, 1, 2177, 128, "bf16", (2177,)),
+    # 32 query rows per KV head (G = 8, nq = 4), short and long caches
+    DecodeWorkload("rows32_cluster", 1, 16, 2, 4, 900, 64, "bf16", (900,)),
+    DecodeWorkload("rows32_split", 2, 16, 2, 4, 4096, 64, "bf16", (4096, 1500)),
 ]
 
 

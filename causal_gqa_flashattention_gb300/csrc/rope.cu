@@ -33,98 +33,87 @@ __global__ void __launch_bounds__(256) rope_table_kernel(float2* __restrict__ cs
   cs[idx] = make_float2(static_cast<float>(c), static_cast<float>(s));
 }
 
+// 16 bytes of a row, kept as loaded (4 registers) until it is rotated:
+// E elements, E / 2 pairs turned by the pairs' (cos, sin) in r.
 template <typename T>
-struct Chunk;  // 16 bytes of a row as fp32 values
+struct Chunk;
 template <>
 struct Chunk<__nv_bfloat16> {
   static constexpr int E = 8;
-  __device__ static void load(const __nv_bfloat16* p, float* v) {
-    const uint4 u = *reinterpret_cast<const uint4*>(p);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  __device__ static uint4 rotate(uint4 u, const float2* r) {
+    uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      v[2 * k] = __uint_as_float(w[k] << 16);
-      v[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
-    }
-  }
-  __device__ static void store(__nv_bfloat16* p, const float* v) {
-    uint32_t w[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+      const float a = __uint_as_float(w[k] << 16), b = __uint_as_float(w[k] & 0xffff0000u);
+      const __nv_bfloat162 h =
+          __floats2bfloat162_rn(fmaf(a, r[k].x, -(b * r[k].y)), fmaf(a, r[k].y, b * r[k].x));
       w[k] = *reinterpret_cast<const uint32_t*>(&h);
     }
-    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    return make_uint4(w[0], w[1], w[2], w[3]);
   }
 };
 template <>
 struct Chunk<float> {
   static constexpr int E = 4;
-  __device__ static void load(const float* p, float* v) {
-    const float4 u = *reinterpret_cast<const float4*>(p);
-    v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
-  }
-  __device__ static void store(float* p, const float* v) {
-    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  __device__ static uint4 rotate(uint4 u, const float2* r) {
+    const float a0 = __uint_as_float(u.x), b0 = __uint_as_float(u.y);
+    const float a1 = __uint_as_float(u.z), b1 = __uint_as_float(u.w);
+    return make_uint4(__float_as_uint(fmaf(a0, r[0].x, -(b0 * r[0].y))),
+                      __float_as_uint(fmaf(a0, r[0].y, b0 * r[0].x)),
+                      __float_as_uint(fmaf(a1, r[1].x, -(b1 * r[1].y))),
+                      __float_as_uint(fmaf(a1, r[1].y, b1 * r[1].x)));
   }
 };
 
 // Thread = (position n, 16-byte column chunk) x a group of kRopeHeads
-// heads: it loads the chunk's (cos, sin) pairs once and reuses them for the
-// same chunk of row n of each of its heads, with all of those rows' loads
-// in flight before the first store.  Heads [0, h0) are rows of x0 -> y0
-// (Q), heads [h0, h0 + h1) rows of x1 -> y1 (K); each head has N rows.
+// heads: the heads' chunks are all loaded before the chunk's (cos, sin)
+// pairs, which serve every head, and before the first store.  Heads
+// [0, h0) are rows of x0 -> y0 (Q), heads [h0, h0 + h1) rows of x1 -> y1
+// (K); each head has N rows.  Chunks stay packed (4 registers each) until
+// they are rotated.
 #ifndef NEA_ROPE_HEADS
 #define NEA_ROPE_HEADS 4
 #endif
 constexpr int kRopeHeads = NEA_ROPE_HEADS;
 
 template <typename T>
-__global__ void __launch_bounds__(256) rope_rotate_kernel(const T* __restrict__ x0, T* y0,
-                                                          long long h0, const T* __restrict__ x1,
-                                                          T* y1, long long h1,
-                                                          const float2* __restrict__ cs, int N,
-                                                          int d) {
+__global__ void __launch_bounds__(256)
+    rope_rotate_kernel(const T* __restrict__ x0, T* y0, long long h0, const T* __restrict__ x1,
+                       T* y1, long long h1, const float2* __restrict__ cs, int N, int d) {
   constexpr int E = Chunk<T>::E;
   const int cpr = d / E;  // chunks per row
   const long long c = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
   if (c >= static_cast<long long>(N) * cpr) return;
   const int n = static_cast<int>(c / cpr);
   const int col = static_cast<int>(c - static_cast<long long>(n) * cpr) * E;
-  float2 r[E / 2];
-  const float4* t = reinterpret_cast<const float4*>(cs + static_cast<size_t>(n) * (d / 2) + col / 2);
-#pragma unroll
-  for (int k = 0; k < E / 4; ++k) {  // two pairs per 16-byte load
-    const float4 w = __ldg(t + k);
-    r[2 * k] = make_float2(w.x, w.y);
-    r[2 * k + 1] = make_float2(w.z, w.w);
-  }
+  // element offset of (head h, row n, chunk col) within x0/y0 or x1/y1
+  auto off = [&](long long h) {
+    return ((h < h0 ? h : h - h0) * N + n) * static_cast<long long>(d) + col;
+  };
   for (long long hb = static_cast<long long>(blockIdx.y) * kRopeHeads; hb < h0 + h1;
        hb += static_cast<long long>(gridDim.y) * kRopeHeads) {
-  float v[kRopeHeads][E];
+    uint4 v[kRopeHeads];
 #pragma unroll
-  for (int u = 0; u < kRopeHeads; ++u) {
-    const long long h = hb + u;
-    if (h < h0 + h1) {
-      const T* x = h < h0 ? x0 + (h * N + n) * static_cast<long long>(d)
-                          : x1 + ((h - h0) * N + n) * static_cast<long long>(d);
-      Chunk<T>::load(x + col, v[u]);
+    for (int u = 0; u < kRopeHeads; ++u) {
+      const long long h = hb + u;
+      if (h < h0 + h1)
+        v[u] = __ldg(reinterpret_cast<const uint4*>((h < h0 ? x0 : x1) + off(h)));
     }
-  }
+    float2 r[E / 2];
+    const float4* t =
+        reinterpret_cast<const float4*>(cs + static_cast<size_t>(n) * (d / 2) + col / 2);
 #pragma unroll
-  for (int u = 0; u < kRopeHeads; ++u) {
-    const long long h = hb + u;
-    if (h >= h0 + h1) continue;
-#pragma unroll
-    for (int k = 0; k < E / 2; ++k) {
-      const float a = v[u][2 * k], b = v[u][2 * k + 1];
-      v[u][2 * k] = fmaf(a, r[k].x, -(b * r[k].y));
-      v[u][2 * k + 1] = fmaf(a, r[k].y, b * r[k].x);
+    for (int k = 0; k < E / 4; ++k) {  // two pairs per 16-byte load
+      const float4 w = __ldg(t + k);
+      r[2 * k] = make_float2(w.x, w.y);
+      r[2 * k + 1] = make_float2(w.z, w.w);
     }
-    T* y = h < h0 ? y0 + (h * N + n) * static_cast<long long>(d)
-                  : y1 + ((h - h0) * N + n) * static_cast<long long>(d);
-    Chunk<T>::store(y + col, v[u]);
-  }
+#pragma unroll
+    for (int u = 0; u < kRopeHeads; ++u) {
+      const long long h = hb + u;
+      if (h < h0 + h1)
+        *reinterpret_cast<uint4*>((h < h0 ? y0 : y1) + off(h)) = Chunk<T>::rotate(v[u], r);
+    }
   }
 }
 

@@ -114,7 +114,11 @@ __global__ void __launch_bounds__(kChunk) decode_partial_kernel(const __grid_con
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  __shared__ __align__(8) uint64_t full[STAGES];
+  // K and V of a stage land on separate barriers: K is released (and the
+  // stage's next K issued) once the scores have read it, while P V still
+  // reads V, so that each load's latency hides under compute of the chunk
+  // before the one that needs it
+  __shared__ __align__(8) uint64_t fullK[STAGES], fullV[STAGES];
   __shared__ int abort_sh;
   float* q_s = reinterpret_cast<float*>(smem + 2 * STAGES * TILE);  // [RM][D], log2 units
   float* p_s = q_s + RM * D;                                        // [RM][kChunk]
@@ -132,26 +136,38 @@ __global__ void __launch_bounds__(kChunk) decode_partial_kernel(const __grid_con
   volatile int* abort = &abort_sh;
   auto sK = [&](int s) { return smem + 2 * s * TILE; };
   auto sV = [&](int s) { return smem + (2 * s + 1) * TILE; };
-  auto issue = [&](int it) {  // thread 0: chunk cb + it into stage it % STAGES
+  // thread 0: K (V) of chunk cb + it into stage it % STAGES
+  auto issue_k = [&](int it) {
     const int s = it % STAGES;
-    const uint32_t bar = smem_u32(&full[s]);
-    mbar_expect_tx(bar, 2 * TILE);
-    for (int k = 0; k < NBLK; ++k) {
+    const uint32_t bar = smem_u32(&fullK[s]);
+    mbar_expect_tx(bar, TILE);
+    for (int k = 0; k < NBLK; ++k)
       tma_load_3d(smem_u32(sK(s) + k * BLK), &a.tmK, bar, k * (128 / ES), (cb + it) * kChunk, bg);
+  };
+  auto issue_v = [&](int it) {
+    const int s = it % STAGES;
+    const uint32_t bar = smem_u32(&fullV[s]);
+    mbar_expect_tx(bar, TILE);
+    for (int k = 0; k < NBLK; ++k)
       tma_load_3d(smem_u32(sV(s) + k * BLK), &a.tmV, bar, k * (128 / ES), (cb + it) * kChunk, bg);
-    }
   };
   if (tid == 0) {
     abort_sh = 0;
-    for (int s = 0; s < STAGES; ++s) mbar_init(smem_u32(&full[s]), 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&fullK[s]), 1);
+      mbar_init(smem_u32(&fullV[s]), 1);
+    }
     fence_barrier_init();
     prefetch_tmap(&a.tmK);
     prefetch_tmap(&a.tmV);
   }
   __syncthreads();
-  int issued = 0;  // chunks whose loads thread 0 has issued
+  int issued_k = 0, issued_v = 0;  // chunks whose K (V) loads thread 0 has issued
   if (tid == 0)
-    for (; issued < STAGES && issued < n; ++issued) issue(issued);
+    for (; issued_k < STAGES && issued_k < n; ++issued_k, ++issued_v) {
+      issue_k(issued_k);
+      issue_v(issued_v);
+    }
   // query rows r = gi * nq + t of heads g*G + gi (absent rows: zeros)
   const T* Q = static_cast<const T*>(a.Q);
   const float cq = a.scale * kLog2e;
@@ -181,7 +197,7 @@ __global__ void __launch_bounds__(kChunk) decode_partial_kernel(const __grid_con
     const int c0 = (cb + it) * kChunk;
     const int jmax = min(kChunk, L - c0);  // valid rows of this chunk
     // every thread waits itself; the CTA agrees before it goes on
-    ok = __syncthreads_and(mbar_wait(smem_u32(&full[s]), (it / STAGES) & 1, abort, 90, a.status));
+    ok = __syncthreads_and(mbar_wait(smem_u32(&fullK[s]), (it / STAGES) & 1, abort, 90, a.status));
     if (!ok) break;
     // scores of cache row c0 + tid, read from its swizzled row
     const int r8 = tid & 7;
@@ -212,16 +228,6 @@ __global__ void __launch_bounds__(kChunk) decode_partial_kernel(const __grid_con
         }
       }
     }
-    // rows past L may hold anything: zero their V so that P V stays finite
-    if (tid >= jmax) {
-      uint8_t* vrow = sV(s) + tid * 128;
-#pragma unroll
-      for (int bl = 0; bl < NBLK; ++bl)
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          *reinterpret_cast<uint4*>(vrow + bl * BLK + (k << 4)) = make_uint4(0u, 0u, 0u, 0u);
-      fence_proxy_async();  // ordered before the TMA that refills this stage
-    }
     const int kj = c0 + tid;
     float sc[RM];
 #pragma unroll
@@ -233,7 +239,21 @@ __global__ void __launch_bounds__(kChunk) decode_partial_kernel(const __grid_con
       for (int off = 16; off > 0; off >>= 1) sv = fmaxf(sv, __shfl_xor_sync(0xffffffffu, sv, off));
       if (lane == 0) red[warp * RM + r] = sv;
     }
-    __syncthreads();
+    __syncthreads();  // K of stage s fully read: refill it
+    if (tid == 0 && issued_k < n) issue_k(issued_k++);
+    ok = __syncthreads_and(mbar_wait(smem_u32(&fullV[s]), (it / STAGES) & 1, abort, 92, a.status));
+    if (!ok) break;
+    // rows past L may hold anything: zero their V so that P V stays finite
+    // (read after the next barrier)
+    if (tid >= jmax) {
+      uint8_t* vrow = sV(s) + tid * 128;
+#pragma unroll
+      for (int bl = 0; bl < NBLK; ++bl)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          *reinterpret_cast<uint4*>(vrow + bl * BLK + (k << 4)) = make_uint4(0u, 0u, 0u, 0u);
+      fence_proxy_async();  // ordered before the TMA that refills this stage
+    }
 #pragma unroll
     for (int r = 0; r < RM; ++r) {
       const float m = fmaxf(fmaxf(red[r], red[RM + r]), fmaxf(red[2 * RM + r], red[3 * RM + r]));
@@ -336,14 +356,18 @@ __global__ void __launch_bounds__(kChunk) decode_partial_kernel(const __grid_con
         m_run[i] = mn;
       }
     }
-    __syncthreads();  // stage s fully read: refill it
-    if (tid == 0 && issued < n) issue(issued++);
+    __syncthreads();  // V of stage s fully read: refill it
+    if (tid == 0 && issued_v < n) issue_v(issued_v++);
   }
   if (!ok) {
-    // unwinding: let this CTA's copies land before it exits
-    if (tid == 0)
-      for (int it = issued > STAGES ? issued - STAGES : 0; it < issued; ++it)
-        mbar_wait_drain(smem_u32(&full[it % STAGES]), (it / STAGES) & 1, 91, a.status);
+    // unwinding: let this CTA's copies land before it exits (the last load
+    // issued into each stage, K and V)
+    if (tid == 0) {
+      for (int it = issued_k > STAGES ? issued_k - STAGES : 0; it < issued_k; ++it)
+        mbar_wait_drain(smem_u32(&fullK[it % STAGES]), (it / STAGES) & 1, 91, a.status);
+      for (int it = issued_v > STAGES ? issued_v - STAGES : 0; it < issued_v; ++it)
+        mbar_wait_drain(smem_u32(&fullV[it % STAGES]), (it / STAGES) & 1, 93, a.status);
+    }
     if (!CLUSTER) return;
   }
   if constexpr (CLUSTER) {
@@ -468,9 +492,10 @@ __global__ void __launch_bounds__(kCombine) decode_combine_kernel(const DecodeAr
 template <typename T, int D, int RM>
 cudaError_t launch_partial(DecodeArgs& a, int sms, cudaStream_t stream) {
   constexpr int TILE = kChunk * D * static_cast<int>(sizeof(T));
-  // One stage: each CTA then needs half the shared memory, and more CTAs per
-  // SM (whose chunks interleave) hide load latency better than a second
-  // stage per CTA does (measured: 153 vs 161 us on a 537 MB cache).
+  // One stage: each CTA then needs the least shared memory, and more CTAs
+  // per SM (whose chunks interleave) hide load latency better than deeper
+  // rings do (measured on a 537 MB cache, K and V on separate barriers:
+  // 148 us with one stage, 164 with two, 197 with three).
   constexpr int STAGES = 1;
   const int smem = 1024 + 2 * STAGES * TILE + (RM * D + RM * kChunk + 8 * RM) * 4 +
                    (RM == 4 ? 16 * D * 4 : 0);

@@ -100,9 +100,9 @@ __device__ __forceinline__ int cache_len(const DecodeArgs& a, int b) {
 // CLUSTER (a short cache): the splits of one (batch, KV head) form a thread-
 // block cluster (gridDim.x = the splits = the cluster's size).  Each leaves
 // its running (max, sum, O) per row in its own shared memory; after a
-// cluster barrier, rank 0 folds them together through distributed shared
-// memory and writes O and LSE: one launch, no partials in global memory, no
-// combine kernel.  A split past its element's cache, and a CTA unwinding
+// cluster barrier, each rank folds one slice of the outputs over all the
+// splits through distributed shared memory and writes its O and LSE
+// values: one launch, no partials in global memory, no combine kernel.  A split past its element's cache, and a CTA unwinding
 // after a timeout, still meet the cluster at both barriers.
 template <typename T, int D, int RM, int STAGES, bool CLUSTER>
 __global__ void __launch_bounds__(kChunk) decode_partial_kernel(const __grid_constant__ DecodeArgs a) {
@@ -392,11 +392,14 @@ __global__ void __launch_bounds__(kChunk) decode_partial_kernel(const __grid_con
       }
     }
     cluster_sync();
-    if (split == 0 && ok) {
-      // rank 0: fold the splits row by row (thread = column, rows in turn)
+    if (ok) {
+      // every rank folds its own slice of the R x D outputs across the
+      // splits (thread = one output element)
       const uint32_t o_base = smem_u32(cl_o), ml_base = smem_u32(cl_ml);
       const int nsp = gridDim.x;
-      for (int e = tid; e < R * D; e += kChunk) {
+      const int per = (R * D + nsp - 1) / nsp;
+      const int e_end = min(R * D, (split + 1) * per);
+      for (int e = split * per + tid; e < e_end; e += kChunk) {
         const int r = e / D, col = e % D;
         float M = -INFINITY;
         for (int q = 0; q < nsp; ++q)
@@ -414,7 +417,7 @@ __global__ void __launch_bounds__(kChunk) decode_partial_kernel(const __grid_con
         if (col == 0) a.lse[row] = (M + log2f(lt)) * kLn2;
       }
     }
-    cluster_sync();  // the other splits' shared memory stays until rank 0 has read it
+    cluster_sync();  // each split's shared memory stays until every rank has read it
   } else {
 #pragma unroll
   for (int i = 0; i < RW; ++i) {

@@ -729,7 +729,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
     };
     // this thread's 64 bytes of the dS'^T row: block q0 / 64, chunks from (q0 % 64) / 8
     const int dsblk = q0 / 64, dsch0 = (q0 % 64) / 8;
-    constexpr bool kDeferDs = false;
     bool ok = true;
     for (int n = 0; n < nsteps; ++n) {
       const int bb = n % DSST;
@@ -777,14 +776,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
         make_p(true);
       else
         make_p(false);
-      // With two dS buffers, the previous step's dS'^T stores are released
-      // here, after this step's P: by now they have completed, so the proxy
-      // fence does not wait for them.
-      if (kDeferDs && n > 0) {
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(dsfull((n - 1) % DSST));
-      }
       tr.ev(38);
       // P^T_n goes into this group's S^T columns, already read; S^T_n was
       // only issued after dV_{n-1} had read P^T_{n-1} there
@@ -838,21 +829,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1) bwd_main_kernel(const _
       for (int c4 = 0; c4 < 4; ++c4)
         *reinterpret_cast<uint4*>(dsrow + (((dsch0 + c4) ^ (kr & 7)) << 4)) =
             make_uint4(o[4 * c4], o[4 * c4 + 1], o[4 * c4 + 2], o[4 * c4 + 3]);
-      if (!kDeferDs) {
-        if constexpr (C::DK_TS) {
-          tmem_st_wait();
-          tc_fence_before();
-        }
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(dsfull(bb));
+      if constexpr (C::DK_TS) {
+        tmem_st_wait();
+        tc_fence_before();
       }
-      tr.ev(35);
-    }
-    if (kDeferDs && ok && nsteps > 0) {  // release the last step's dS'^T
       fence_proxy_async();
       __syncwarp();
-      if (lane == 0) mbar_arrive(dsfull((nsteps - 1) % DSST));
+      if (lane == 0) mbar_arrive(dsfull(bb));
+      tr.ev(35);
     }
     // epilogue: groups 0, 1 write the two column halves of dV, groups 2, 3
     // those of dK, for this CTA's key rows
